@@ -1,0 +1,260 @@
+"""CPU oracle for the layer operators RMSNorm, rotary position embedding and SwiGLU.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The CUDA library never calls it and it never calls the CUDA library:
+the two share no code, no constants and no helpers.
+
+Everything here is plain numpy in float64, single-threaded (no BLAS call is
+made), written as the textbook definition of each operator, one step per line,
+so that it can be read against the sources by eye.  The sources name the
+operators and their hyper-parameters but do not print their formulas:
+
+* "Fast-LLM: 高效大语言模型训练框架", §三 技术架构, table "Transformer Block 结构"
+  (normalization is LayerNorm / RMSNorm; the mixer is attention with RoPE; the
+  MLP is gated or not, with SiLU / GeLU / ReLU) and §三 "训练配置示例" (``rms_norm``
+  with ``epsilon``, ``rotary: type: default, theta``, ``gated: true,
+  activation: silu``).
+* "LLaMA-Factory Kernels 系统", the kernel table (fused RMSNorm, SwiGLU and RoPE
+  operators).
+* "Kernels（自定义内核）" (transformers docs), §Liger (RMSNorm, RoPE and SwiGLU
+  fused into single kernels, for training, so with backward passes).
+
+Readings taken where the sources are silent (each is listed with its reason in
+the design notes of the repository):
+
+* RMSNorm: ``rstd = 1/sqrt(mean(h^2) + eps)`` (eps inside the root), no mean
+  subtraction, no bias, the weight multiplies (not ``1 + w``).
+* Fused residual: ``h = x + residual`` is rounded to the I/O precision first;
+  the rounded ``h`` is both the residual-stream output and what is normalised.
+* RoPE: rotate-half pairing ``(i, i + D/2)``; frequencies
+  ``theta_i = theta ** (-2 i / D)``; angle ``pos * theta_i``; the same rotation
+  for every head of a token, Q and K alike; backward is the inverse rotation.
+* SwiGLU: ``out = silu(gate) * up`` with ``silu(g) = g / (1 + exp(-g))``;
+  gate and up are two separate tensors.
+
+Pins for every function live in ``tests/test_oracle_pins.py``.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "round_to_bf16",
+    "round_to_f32",
+    "round_io",
+    "rmsnorm_fwd",
+    "rmsnorm_bwd",
+    "rmsnorm_dw",
+    "rope_inv_freq",
+    "rope_fwd",
+    "rope_bwd",
+    "silu",
+    "swiglu_fwd",
+    "swiglu_bwd",
+    "positions_from_doc_lengths",
+    "positions_from_cu_seqlens",
+]
+
+
+# ---------------------------------------------------------------------------
+# Rounding to the I/O precision
+# ---------------------------------------------------------------------------
+
+def round_to_bf16(a):
+    """Round float64 values to the nearest bfloat16 value, ties to even.
+
+    bfloat16 keeps 8 significant bits (1 implicit + 7 stored) with float32's
+    exponent range.  Written from that definition: split ``a = m * 2**e`` with
+    ``0.5 <= |m| < 1``, scale ``m`` to an integer part of 8 bits, round half to
+    even, scale back.  Values below float32's normal range and overflow to
+    infinity are outside what this oracle is used for (inputs are O(1)).
+    """
+    a = np.asarray(a, dtype=np.float64)
+    m, e = np.frexp(a)
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def round_to_f32(a):
+    """Round float64 values to the nearest float32 value (ties to even)."""
+    return np.asarray(a, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def round_io(a, io):
+    """Round to the I/O precision ``io`` in {"bf16", "f32", None}; None = keep float64."""
+    if io is None:
+        return np.asarray(a, dtype=np.float64)
+    if io == "bf16":
+        return round_to_bf16(a)
+    if io == "f32":
+        return round_to_f32(a)
+    raise ValueError(f"unknown io precision {io!r}")
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm with fused residual add
+# ("Fast-LLM: 高效大语言模型训练框架", §三 Transformer Block 结构 and 训练配置示例)
+# ---------------------------------------------------------------------------
+
+def rmsnorm_fwd(x, residual, weight, eps, io=None):
+    """RMSNorm forward over the last axis, with an optional residual add first.
+
+    x, residual: [T, H] float64 (residual may be None); weight: [H].
+    Returns ``(y, h, rstd)``:
+      h    = round_io(x + residual)   the residual-stream output (x if no residual)
+      rstd = 1 / sqrt(mean(h**2) + eps)   per row, [T]
+      y    = weight * h * rstd        exact, before any output rounding
+    """
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(weight, dtype=np.float64)
+    if residual is None:
+        h = x
+    else:
+        h = round_io(x + np.asarray(residual, dtype=np.float64), io)
+    ms = np.mean(h * h, axis=-1)
+    rstd = 1.0 / np.sqrt(ms + eps)
+    y = w * h * rstd[..., None]
+    return y, h, rstd
+
+
+def rmsnorm_bwd(dy, dres, h, weight, eps):
+    """RMSNorm backward: gradient of ``(y, h)`` back to the pre-add input.
+
+    dy: [T, H] gradient of y; dres: [T, H] gradient arriving on the
+    residual-stream output h (None = zero); h: [T, H] the normalised input;
+    weight: [H].  rstd is recomputed from h.  With n = h * rstd and
+    g = dy * weight, the chain rule through y = weight * n gives
+      dh = rstd * (g - n * mean(g * n))       per row
+      dx = dh + dres                          (= gradient of x and of residual)
+      dW = sum over rows of dy * n            [H]
+    Returns ``(dx, dW)``.
+    """
+    dy = np.asarray(dy, dtype=np.float64)
+    h = np.asarray(h, dtype=np.float64)
+    w = np.asarray(weight, dtype=np.float64)
+    rstd = 1.0 / np.sqrt(np.mean(h * h, axis=-1) + eps)
+    n = h * rstd[..., None]
+    g = dy * w
+    c = np.mean(g * n, axis=-1)
+    dx = rstd[..., None] * (g - n * c[..., None])
+    if dres is not None:
+        dx = dx + np.asarray(dres, dtype=np.float64)
+    dw = np.sum(dy * n, axis=0)
+    return dx, dw
+
+
+def rmsnorm_dw(dy, h, eps, rows_per_chunk=4096):
+    """Weight gradient alone, ``sum_t dy_t * h_t * rstd_t``, streamed over row chunks.
+
+    Same arithmetic as the dW of :func:`rmsnorm_bwd`, for inputs too large to
+    hold in float64 at once (arrays may be float32 or bfloat16-valued float32).
+    """
+    T, H = dy.shape
+    dw = np.zeros(H, dtype=np.float64)
+    for t0 in range(0, T, rows_per_chunk):
+        hb = np.asarray(h[t0:t0 + rows_per_chunk], dtype=np.float64)
+        dyb = np.asarray(dy[t0:t0 + rows_per_chunk], dtype=np.float64)
+        rstd = 1.0 / np.sqrt(np.mean(hb * hb, axis=-1) + eps)
+        dw += np.sum(dyb * hb * rstd[:, None], axis=0)
+    return dw
+
+
+# ---------------------------------------------------------------------------
+# Rotary position embedding on Q and K
+# ("Fast-LLM: 高效大语言模型训练框架", §三 框架结构 (attention with RoPE) and
+#  训练配置示例 (rotary type default, theta); "LLaMA-Factory Kernels 系统")
+# ---------------------------------------------------------------------------
+
+def rope_inv_freq(D, theta):
+    """Per-pair frequencies ``theta ** (-2 i / D)`` for i = 0 .. D/2 - 1."""
+    i = np.arange(D // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * i / D)
+
+
+def _rope_rotate(x, positions, theta, sign):
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    half = D // 2
+    freq = rope_inv_freq(D, theta)                                  # [D/2]
+    angle = np.asarray(positions, dtype=np.float64)[:, None] * freq  # [T, D/2]
+    cos = np.cos(angle)[:, None, :]                                 # [T, 1, D/2]
+    sin = sign * np.sin(angle)[:, None, :]
+    x1 = x[..., :half]
+    x2 = x[..., half:]
+    out = np.empty_like(x)
+    out[..., :half] = x1 * cos - x2 * sin
+    out[..., half:] = x2 * cos + x1 * sin
+    return out
+
+
+def rope_fwd(x, positions, theta):
+    """Rotate every head of token t by angle ``positions[t] * theta_i`` on pair (i, i + D/2).
+
+    x: [T, heads, D] float64; positions: [T] integers.  Returns the rotated
+    array.  Q and K are each passed through this with the same positions.
+    """
+    return _rope_rotate(x, positions, theta, +1.0)
+
+
+def rope_bwd(dout, positions, theta):
+    """Gradient of :func:`rope_fwd`: the transpose (= inverse) rotation, angle negated."""
+    return _rope_rotate(dout, positions, theta, -1.0)
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU  (gated MLP with SiLU: "Fast-LLM: 高效大语言模型训练框架", §三 支持的 MLP 变体
+#  and 训练配置示例; "LLaMA-Factory Kernels 系统"; "Kernels（自定义内核）" §Liger)
+# ---------------------------------------------------------------------------
+
+def _sigmoid(g):
+    return 1.0 / (1.0 + np.exp(-g))
+
+
+def silu(g):
+    """SiLU, ``g * sigmoid(g)``."""
+    g = np.asarray(g, dtype=np.float64)
+    return g * _sigmoid(g)
+
+
+def swiglu_fwd(gate, up):
+    """``out = silu(gate) * up`` elementwise."""
+    gate = np.asarray(gate, dtype=np.float64)
+    up = np.asarray(up, dtype=np.float64)
+    return silu(gate) * up
+
+
+def swiglu_bwd(dout, gate, up):
+    """Gradients of :func:`swiglu_fwd`.
+
+    With s = sigmoid(g): d silu/dg = s + g * s * (1 - s) = s * (1 + g * (1 - s)), so
+      dgate = dout * up * s * (1 + g * (1 - s))
+      dup   = dout * g * s
+    Returns ``(dgate, dup)``.
+    """
+    dout = np.asarray(dout, dtype=np.float64)
+    g = np.asarray(gate, dtype=np.float64)
+    u = np.asarray(up, dtype=np.float64)
+    s = _sigmoid(g)
+    dgate = dout * u * s * (1.0 + g * (1.0 - s))
+    dup = dout * g * s
+    return dgate, dup
+
+
+# ---------------------------------------------------------------------------
+# Positions for packed documents ("Fast-LLM: 高效大语言模型训练框架", §三 训练配置示例:
+#  micro_batch_size counted in tokens, maximum_document_length; §三 数据管道)
+# ---------------------------------------------------------------------------
+
+def positions_from_doc_lengths(lengths):
+    """Position of each token inside its own document: 0, 1, ..., L-1 per document, concatenated."""
+    parts = [np.arange(int(L), dtype=np.int64) for L in lengths]
+    if not parts:
+        return np.zeros(0, dtype=np.int64)
+    return np.concatenate(parts)
+
+
+def positions_from_cu_seqlens(cu_seqlens):
+    """Same, from cumulative document boundaries ``cu_seqlens`` (cu[0] = 0, cu[-1] = T)."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    return positions_from_doc_lengths(cu[1:] - cu[:-1])

@@ -1,0 +1,344 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test fixes the oracle to a closed form, an invariant, a hand-worked value
+(``tests/golden/``), an independent library routine or a finite difference, so
+that a dropped term, a wrong sign, a wrong pairing or a swapped operand in the
+oracle fails at least one of them.  CPU only.
+"""
+
+import cmath
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    out = []
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                out.append([float(v) for v in line.split()])
+    return out
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding
+# ---------------------------------------------------------------------------
+
+def test_bf16_rounding_hand_cases():
+    for num, den, enum, eden in _rows("bf16_rounding.txt"):
+        got = oracle.round_to_bf16(np.array([num / den]))[0]
+        assert got == enum / eden, (num, den, got)
+
+
+def test_bf16_rounding_matches_torch_conversion():
+    # torch's float32 -> bfloat16 cast is an independent round-to-nearest-even.
+    g = torch.Generator().manual_seed(1)
+    v = torch.randn(200000, generator=g) * torch.exp(torch.randn(200000, generator=g) * 4)
+    ref = v.to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_to_bf16(v.to(torch.float64).numpy())
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_sum_rounding_matches_torch_on_bf16_pairs():
+    # h = round(x + r) from double equals torch's (fp32 add, then RNE to bf16):
+    # float32 has more than 2*8+2 bits, so its intermediate rounding is innocuous.
+    g = torch.Generator().manual_seed(2)
+    x = (torch.randn(100000, generator=g) * 3).to(torch.bfloat16)
+    r = (torch.randn(100000, generator=g) * torch.exp(torch.randn(100000, generator=g) * 3)).to(torch.bfloat16)
+    ref = (x.float() + r.float()).to(torch.bfloat16).double().numpy()
+    got = oracle.round_to_bf16(x.double().numpy() + r.double().numpy())
+    assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm forward
+# ---------------------------------------------------------------------------
+
+def test_rmsnorm_single_channel_hand_values():
+    for h, eps, w, y in _rows("rmsnorm_h1.txt"):
+        got, _, _ = oracle.rmsnorm_fwd(np.array([[h]]), None, np.array([w]), eps)
+        assert got[0, 0] == pytest.approx(y, rel=1e-15, abs=1e-15)
+
+
+def test_rmsnorm_unit_rms_closed_form():
+    rng = np.random.default_rng(0)
+    x = rng.normal(size=(7, 33))
+    r = rng.normal(size=(7, 33))
+    w = 1 + 0.1 * rng.normal(size=33)
+    for eps in (0.0, 1e-5, 0.3):
+        y, h, rstd = oracle.rmsnorm_fwd(x, r, w, eps)
+        ms = np.mean(h * h, axis=1)
+        rms = np.sqrt(np.mean((y / w) ** 2, axis=1))
+        assert np.allclose(rms, np.sqrt(ms / (ms + eps)), rtol=1e-13, atol=0)
+        if eps == 0.0:
+            assert np.allclose(rms, 1.0, rtol=1e-13)
+        assert np.array_equal(h, x + r)  # io=None keeps the exact sum
+
+
+def test_rmsnorm_scale_invariance_at_zero_eps():
+    rng = np.random.default_rng(1)
+    x = rng.normal(size=(5, 16))
+    w = rng.normal(size=16)
+    y1, _, _ = oracle.rmsnorm_fwd(x, None, w, 0.0)
+    y2, _, _ = oracle.rmsnorm_fwd(37.5 * x, None, w, 0.0)
+    assert np.allclose(y1, y2, rtol=1e-13, atol=1e-14)
+
+
+def test_rmsnorm_residual_rounded_before_normalising():
+    # With bf16 I/O the stored h is the bf16 sum, and y normalises that h.
+    x = np.array([[1.0, 1.0]])
+    r = np.array([[2.0 ** -8, 0.0]])  # 1 + 2^-8 is a tie: rounds to 1
+    y, h, rstd = oracle.rmsnorm_fwd(x, r, np.ones(2), 0.0, io="bf16")
+    assert np.array_equal(h, [[1.0, 1.0]])
+    assert np.allclose(y, [[1.0, 1.0]], rtol=1e-15)
+    assert rstd[0] == pytest.approx(1.0, rel=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm backward
+# ---------------------------------------------------------------------------
+
+def _rms_loss(x, r, w, eps, dy, dres):
+    y, h, _ = oracle.rmsnorm_fwd(x, r, w, eps)
+    return float(np.sum(dy * y) + np.sum(dres * h))
+
+
+@pytest.mark.parametrize("H", [1, 5, 8])
+def test_rmsnorm_bwd_central_differences(H):
+    rng = np.random.default_rng(10 + H)
+    T, eps, d = 3, 1e-2, 1e-6
+    x = rng.normal(size=(T, H))
+    r = rng.normal(size=(T, H))
+    w = 1 + 0.1 * rng.normal(size=H)
+    dy = rng.normal(size=(T, H))
+    dres = rng.normal(size=(T, H))
+    _, h, _ = oracle.rmsnorm_fwd(x, r, w, eps)
+    dx, dw = oracle.rmsnorm_bwd(dy, dres, h, w, eps)
+    fd_x = np.zeros_like(x)
+    for idx in np.ndindex(x.shape):
+        xp = x.copy(); xp[idx] += d
+        xm = x.copy(); xm[idx] -= d
+        fd_x[idx] = (_rms_loss(xp, r, w, eps, dy, dres) - _rms_loss(xm, r, w, eps, dy, dres)) / (2 * d)
+    fd_w = np.zeros_like(w)
+    for j in range(H):
+        wp = w.copy(); wp[j] += d
+        wm = w.copy(); wm[j] -= d
+        fd_w[j] = (_rms_loss(x, r, wp, eps, dy, dres) - _rms_loss(x, r, wm, eps, dy, dres)) / (2 * d)
+    assert np.allclose(dx, fd_x, rtol=1e-7, atol=1e-8)
+    assert np.allclose(dw, fd_w, rtol=1e-7, atol=1e-8)
+
+
+def test_rmsnorm_bwd_orthogonality_closed_form():
+    # sum_j dh_j h_j = rstd * sum(g h) * eps / (ms + eps); zero when eps = 0.
+    rng = np.random.default_rng(3)
+    h = rng.normal(size=(4, 12))
+    w = rng.normal(size=12)
+    dy = rng.normal(size=(4, 12))
+    for eps in (0.0, 0.5):
+        dh, _ = oracle.rmsnorm_bwd(dy, None, h, w, eps)
+        ms = np.mean(h * h, axis=1)
+        rstd = 1 / np.sqrt(ms + eps)
+        lhs = np.sum(dh * h, axis=1)
+        rhs = rstd * np.sum(dy * w * h, axis=1) * eps / (ms + eps)
+        assert np.allclose(lhs, rhs, rtol=1e-10, atol=1e-12)
+
+
+def test_rmsnorm_dw_brute_force_and_chunked():
+    rng = np.random.default_rng(4)
+    T, H, eps = 9, 6, 1e-5
+    h = rng.normal(size=(T, H))
+    dy = rng.normal(size=(T, H))
+    w = rng.normal(size=H)
+    _, dw = oracle.rmsnorm_bwd(dy, None, h, w, eps)
+    brute = [0.0] * H
+    for t in range(T):
+        rstd = 1.0 / math.sqrt(sum(v * v for v in h[t]) / H + eps)
+        for j in range(H):
+            brute[j] += dy[t, j] * h[t, j] * rstd
+    assert np.allclose(dw, brute, rtol=1e-13)
+    assert np.allclose(oracle.rmsnorm_dw(dy, h, eps, rows_per_chunk=2), brute, rtol=1e-13)
+
+
+def test_rmsnorm_dw_sum_of_shards_equals_full():
+    # The weight gradient of a token-sharded batch is the sum of per-shard gradients.
+    rng = np.random.default_rng(5)
+    T, H, eps = 40, 10, 1e-6
+    h = rng.normal(size=(T, H))
+    dy = rng.normal(size=(T, H))
+    full = oracle.rmsnorm_dw(dy, h, eps)
+    cuts = [0, 7, 19, 33, 40]
+    parts = sum(oracle.rmsnorm_dw(dy[a:b], h[a:b], eps) for a, b in zip(cuts[:-1], cuts[1:]))
+    assert np.allclose(parts, full, rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# RoPE
+# ---------------------------------------------------------------------------
+
+def test_rope_hand_values_d4():
+    for row in _rows("rope_d4.txt"):
+        pos, x, y = row[0], np.array(row[1:5]), np.array(row[5:9])
+        got = oracle.rope_fwd(x.reshape(1, 1, 4), np.array([pos]), 10000.0)
+        assert np.allclose(got.reshape(4), y, rtol=0, atol=1e-15)
+
+
+def test_rope_inv_freq_values():
+    f = oracle.rope_inv_freq(8, 10000.0)
+    assert np.allclose(f, [1.0, 0.1, 0.01, 0.001], rtol=1e-15)
+
+
+def test_rope_equals_complex_multiplication():
+    # Pair (i, i + D/2) as the complex number x_i + j x_{i+D/2}, turned by exp(j pos theta_i).
+    rng = np.random.default_rng(6)
+    T, Hh, D, theta = 5, 3, 8, 500000.0
+    x = rng.normal(size=(T, Hh, D))
+    pos = rng.integers(0, 20000, size=T)
+    got = oracle.rope_fwd(x, pos, theta)
+    for t in range(T):
+        for hh in range(Hh):
+            for i in range(D // 2):
+                z = complex(x[t, hh, i], x[t, hh, i + D // 2])
+                zr = z * cmath.exp(1j * pos[t] * theta ** (-2.0 * i / D))
+                assert got[t, hh, i] == pytest.approx(zr.real, abs=1e-11)
+                assert got[t, hh, i + D // 2] == pytest.approx(zr.imag, abs=1e-11)
+
+
+def test_rope_position_zero_is_identity_and_norm_preserved():
+    rng = np.random.default_rng(7)
+    x = rng.normal(size=(6, 4, 64))
+    assert np.array_equal(oracle.rope_fwd(x, np.zeros(6), 1e6), x)
+    pos = np.array([1, 2, 255, 4095, 8191, 16383])
+    y = oracle.rope_fwd(x, pos, 1e6)
+    pair_in = x[..., :32] ** 2 + x[..., 32:] ** 2
+    pair_out = y[..., :32] ** 2 + y[..., 32:] ** 2
+    assert np.allclose(pair_in, pair_out, rtol=1e-12)
+
+
+def test_rope_relative_position():
+    rng = np.random.default_rng(8)
+    D, theta = 16, 10000.0
+    q = rng.normal(size=(1, 1, D))
+    k = rng.normal(size=(1, 1, D))
+    for m, n, s in [(5, 2, 100), (0, 9, 3000), (77, 77, 12)]:
+        a = np.sum(oracle.rope_fwd(q, [m], theta) * oracle.rope_fwd(k, [n], theta))
+        b = np.sum(oracle.rope_fwd(q, [m + s], theta) * oracle.rope_fwd(k, [n + s], theta))
+        assert a == pytest.approx(b, rel=1e-10, abs=1e-12)
+
+
+def test_rope_bwd_inverts_fwd_and_is_its_adjoint():
+    rng = np.random.default_rng(9)
+    x = rng.normal(size=(4, 3, 32))
+    g = rng.normal(size=(4, 3, 32))
+    pos = np.array([0, 3, 1000, 16000])
+    y = oracle.rope_fwd(x, pos, 5e5)
+    assert np.allclose(oracle.rope_bwd(y, pos, 5e5), x, rtol=1e-12, atol=1e-12)
+    assert np.sum(y * g) == pytest.approx(np.sum(x * oracle.rope_bwd(g, pos, 5e5)), rel=1e-12)
+    assert np.allclose(oracle.rope_bwd(x, pos, 5e5), oracle.rope_fwd(x, -pos, 5e5), atol=1e-13)
+
+
+def test_rope_d2_is_plain_rotation_by_pos_radians():
+    x = np.array([[[0.3, -1.7]]])
+    for p in (1, 2, 7):
+        y = oracle.rope_fwd(x, [p], 12345.0).reshape(2)
+        c, s = math.cos(p), math.sin(p)
+        assert y[0] == pytest.approx(0.3 * c + 1.7 * s, abs=1e-15)
+        assert y[1] == pytest.approx(-1.7 * c + 0.3 * s, abs=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU
+# ---------------------------------------------------------------------------
+
+def test_swiglu_hand_values():
+    for g, u, out in _rows("silu.txt"):
+        assert oracle.swiglu_fwd(np.array([g]), np.array([u]))[0] == pytest.approx(out, rel=1e-15, abs=1e-16)
+
+
+def test_swiglu_special_cases():
+    dout = np.array([1.5, -2.0])
+    u = np.array([3.0, 0.25])
+    g = np.zeros(2)
+    dgate, dup = oracle.swiglu_bwd(dout, g, u)
+    assert np.array_equal(oracle.swiglu_fwd(g, u), [0.0, 0.0])
+    assert np.allclose(dgate, 0.5 * dout * u, rtol=1e-15)
+    assert np.array_equal(dup, [0.0, 0.0])
+    big = np.array([40.0])
+    assert oracle.swiglu_fwd(big, np.array([2.0]))[0] == pytest.approx(80.0, rel=1e-15)
+    assert oracle.swiglu_fwd(np.array([-40.0]), np.array([2.0]))[0] == pytest.approx(0.0, abs=1e-15)
+
+
+def test_swiglu_scalar_brute_force():
+    rng = np.random.default_rng(11)
+    g = rng.normal(size=50) * 3
+    u = rng.normal(size=50)
+    dout = rng.normal(size=50)
+    out = oracle.swiglu_fwd(g, u)
+    dgate, dup = oracle.swiglu_bwd(dout, g, u)
+    for i in range(50):
+        e = math.exp(-g[i])
+        assert out[i] == pytest.approx(g[i] / (1 + e) * u[i], rel=1e-14, abs=1e-300)
+        # product rule on g / (1 + e^-g): (1 + e + g e) / (1 + e)^2
+        assert dgate[i] == pytest.approx(dout[i] * u[i] * (1 + e + g[i] * e) / (1 + e) ** 2, rel=1e-12, abs=1e-300)
+        assert dup[i] == pytest.approx(dout[i] * g[i] / (1 + e), rel=1e-14, abs=1e-300)
+
+
+def test_swiglu_bwd_central_differences():
+    rng = np.random.default_rng(12)
+    g = rng.normal(size=20) * 2
+    u = rng.normal(size=20)
+    dout = rng.normal(size=20)
+    dgate, dup = oracle.swiglu_bwd(dout, g, u)
+    d = 1e-6
+    for i in range(20):
+        gp = g.copy(); gp[i] += d
+        gm = g.copy(); gm[i] -= d
+        fd = (np.sum(dout * oracle.swiglu_fwd(gp, u)) - np.sum(dout * oracle.swiglu_fwd(gm, u))) / (2 * d)
+        assert dgate[i] == pytest.approx(fd, rel=1e-7, abs=1e-9)
+        up_ = u.copy(); up_[i] += d
+        um = u.copy(); um[i] -= d
+        fd = (np.sum(dout * oracle.swiglu_fwd(g, up_)) - np.sum(dout * oracle.swiglu_fwd(g, um))) / (2 * d)
+        assert dup[i] == pytest.approx(fd, rel=1e-7, abs=1e-9)
+
+
+def test_rope_bwd_central_differences():
+    rng = np.random.default_rng(13)
+    x = rng.normal(size=(2, 2, 8))
+    dout = rng.normal(size=(2, 2, 8))
+    pos = np.array([3, 11])
+    grad = oracle.rope_bwd(dout, pos, 100.0)
+    d = 1e-6
+    for idx in np.ndindex(x.shape):
+        xp = x.copy(); xp[idx] += d
+        xm = x.copy(); xm[idx] -= d
+        fd = (np.sum(dout * oracle.rope_fwd(xp, pos, 100.0)) - np.sum(dout * oracle.rope_fwd(xm, pos, 100.0))) / (2 * d)
+        assert grad[idx] == pytest.approx(fd, rel=1e-7, abs=1e-9)
+
+
+# ---------------------------------------------------------------------------
+# Positions of packed documents
+# ---------------------------------------------------------------------------
+
+def test_positions_brute_force():
+    lengths = [3, 1, 5, 2]
+    pos = oracle.positions_from_doc_lengths(lengths)
+    expect = []
+    for L in lengths:
+        p = 0
+        for _ in range(L):
+            expect.append(p)
+            p += 1
+    assert pos.tolist() == expect
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    assert oracle.positions_from_cu_seqlens(cu).tolist() == expect
+    for start in cu[:-1]:
+        assert pos[start] == 0
+    assert oracle.positions_from_doc_lengths([]).size == 0
