@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Throughput of one fused-layer-operator step on GB300: RMSNorm / RoPE / SwiGLU, forward + backward.
+
+One step = every operator of the path once over one batch of tokens, in training
+order: positions of packed documents -> RMSNorm forward (fused residual add) ->
+RoPE forward on Q and K -> SwiGLU forward -> SwiGLU backward -> RoPE backward ->
+RMSNorm backward (dX and dW partials) -> dW finalize.  Eight launches of the
+library's kernels, called through the C ABI with device pointers.
+
+Prints one JSON line.  ``value`` is tokens per second over all ranks with inputs
+resident in HBM; ``e2e`` is the same step through the same C ABI with the inputs
+in pinned host memory and the outputs read back, copies inside the timed region.
+L2 is flushed (a 2x L2 write) between timed steps.  ``--impl reference`` times
+the float64 CPU oracle on a bounded sample of the same workload instead.
+
+Multi-GPU (torchrun): each rank runs its own replica on its own batch (weak
+scaling, no data-path collective); timing is max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "fwd+bwd tokens/s and achieved HBM GB/s (% of GB300 peak), RMSNorm/RoPE/SwiGLU"
+DEFAULT_WORKLOAD = "qwen3_0p6b"
+FALLBACK_HBM_GBS = 6800.0
+OPS = ["positions", "rmsnorm_fwd", "rope_fwd", "swiglu_fwd", "swiglu_bwd", "rope_bwd",
+       "rmsnorm_bwd", "rmsnorm_dw_finalize"]
+KERNEL_SOURCE = {"positions": "rope.cu", "rmsnorm_fwd": "rmsnorm.cu", "rope_fwd": "rope.cu",
+                 "swiglu_fwd": "swiglu.cu", "swiglu_bwd": "swiglu.cu", "rope_bwd": "rope.cu",
+                 "rmsnorm_bwd": "rmsnorm.cu", "rmsnorm_dw_finalize": "rmsnorm.cu"}
+# DRAM bytes (read + write) per launch from one ncu capture, keyed by workload and
+# operator, with the sha256 of the kernel source they were taken on: a changed
+# kernel reports null until it is captured again.  Summaries live under profiles/.
+NCU_TRAFFIC = {}
+
+
+def _src_sha(op):
+    p = os.path.join(ROOT, "rmsnorm_fwd_bwd_03_gb300", "csrc", KERNEL_SOURCE[op])
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+    def find(obj):
+        if isinstance(obj, dict):
+            for k, v in obj.items():
+                if "hbm" in k.lower() and isinstance(v, (int, float)):
+                    return float(v)
+            for v in obj.values():
+                r = find(v)
+                if r:
+                    return r
+        return None
+    v = find(d)
+    return (v, "measured") if v else (FALLBACK_HBM_GBS, "fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r.split(",") for r in (self.out or "").strip().splitlines() if r.strip()]
+        rows = [[c.strip() for c in r] for r in rows if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][2]), "reasons": sorted(reasons),
+                "power_w_median": statistics.median([num(r[3]) for r in rows if num(r[3]) is not None] or [0]),
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# The step through the C ABI
+# ---------------------------------------------------------------------------
+
+class Step:
+    """Device buffers and the eight C-ABI calls of one fwd + bwd step."""
+
+    def __init__(self, wl, device, seed):
+        import rmsnorm_fwd_bwd_03_gb300 as gb
+        from rmsnorm_fwd_bwd_03_gb300.workload import make_inputs
+        self.gb = gb
+        self.lib = gb.library()
+        self.wl = wl
+        T, H = wl.T, wl.H
+        inp = make_inputs(wl, device, seed=seed)
+        self.inp = inp
+        e = lambda like: torch.empty_like(like)  # noqa: E731
+        self.out = {
+            "positions": torch.empty(T, dtype=torch.int32, device=device),
+            "y": e(inp["x"]), "h": e(inp["x"]),
+            "rstd": torch.empty(T, dtype=torch.float32, device=device),
+            "q_out": e(inp["q"]), "k_out": e(inp["k"]),
+            "out": e(inp["gate"]), "dgate": e(inp["gate"]), "dup": e(inp["up"]),
+            "dq_in": e(inp["dq"]), "dk_in": e(inp["dk"]),
+            "dx": e(inp["x"]), "dw": torch.empty(H, dtype=torch.float32, device=device),
+        }
+        self.P = gb.rmsnorm_bwd_num_partials(T, H, wl.dtype)
+        self.partial = torch.empty((self.P, H), dtype=torch.float32, device=device)
+        self.max_pos = wl.max_pos()
+        self.table = gb.rope_table(self.max_pos, wl.D, wl.theta, device=device)
+        self.io = gb.BF16 if wl.dtype == torch.bfloat16 else gb.F32
+        torch.cuda.synchronize()
+
+    def calls(self, stream_handle):
+        """The eight (name, fn, args) calls of a step on the given stream."""
+        i, o, wl, L = self.inp, self.out, self.wl, self.lib
+        p = lambda t: t.data_ptr()  # noqa: E731
+        T, H = wl.T, wl.H
+        s = stream_handle
+        return [
+            ("positions", L.gbln_positions_from_cu_seqlens,
+             (p(i["cu_seqlens"]), i["cu_seqlens"].numel() - 1, p(o["positions"]), T, s)),
+            ("rmsnorm_fwd", L.gbln_rmsnorm_fwd,
+             (p(i["x"]), p(i["residual"]), p(i["weight"]), p(o["y"]), p(o["h"]), p(o["rstd"]),
+              T, H, wl.eps, self.io, self.io, s)),
+            ("rope_fwd", L.gbln_rope_fwd,
+             (p(i["q"]), p(i["k"]), p(o["q_out"]), p(o["k_out"]), p(o["positions"]), p(self.table),
+              self.max_pos, T, wl.Hq, wl.Hk, wl.D, self.io, s)),
+            ("swiglu_fwd", L.gbln_swiglu_fwd, (p(i["gate"]), p(i["up"]), p(o["out"]), T, wl.I, self.io, s)),
+            ("swiglu_bwd", L.gbln_swiglu_bwd,
+             (p(i["dout"]), p(i["gate"]), p(i["up"]), p(o["dgate"]), p(o["dup"]), T, wl.I, self.io, s)),
+            ("rope_bwd", L.gbln_rope_bwd,
+             (p(i["dq"]), p(i["dk"]), p(o["dq_in"]), p(o["dk_in"]), p(o["positions"]), p(self.table),
+              self.max_pos, T, wl.Hq, wl.Hk, wl.D, self.io, s)),
+            ("rmsnorm_bwd", L.gbln_rmsnorm_bwd,
+             (p(i["dy"]), p(i["dres"]), p(o["h"]), p(i["weight"]), p(o["rstd"]), p(o["dx"]),
+              p(self.partial), self.P, T, H, self.io, self.io, s)),
+            ("rmsnorm_dw_finalize", L.gbln_rmsnorm_dw_finalize,
+             (p(self.partial), self.P, H, p(o["dw"]), 0, s)),
+        ]
+
+    def host_io(self):
+        """Pinned host copies of the step's inputs and outputs (for the end-to-end leg)."""
+        ins = {k: v.cpu().pin_memory() for k, v in self.inp.items()}
+        outs = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in self.out.items()}
+        return ins, outs
+
+
+def run_calls(calls, events=None):
+    if events is None:
+        for name, fn, args in calls:
+            st = fn(*args)
+            if st != 0:
+                raise RuntimeError(f"{name} failed with status {st}")
+        return
+    events[0].record()
+    for k, (name, fn, args) in enumerate(calls):
+        st = fn(*args)
+        if st != 0:
+            raise RuntimeError(f"{name} failed with status {st}")
+        events[k + 1].record()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+# ---------------------------------------------------------------------------
+
+def oracle_step(wl, inp):
+    """One fwd + bwd pass of the oracle over the rows of ``inp`` (float64 numpy arrays)."""
+    import oracle
+    pos = oracle.positions_from_cu_seqlens(inp["cu_seqlens"])
+    y, h, rstd = oracle.rmsnorm_fwd(inp["x"], inp["residual"], inp["weight"], wl.eps, io=wl.io)
+    oracle.rope_fwd(inp["q"], pos, wl.theta)
+    oracle.rope_fwd(inp["k"], pos, wl.theta)
+    oracle.swiglu_fwd(inp["gate"], inp["up"])
+    oracle.swiglu_bwd(inp["dout"], inp["gate"], inp["up"])
+    oracle.rope_bwd(inp["dq"], pos, wl.theta)
+    oracle.rope_bwd(inp["dk"], pos, wl.theta)
+    oracle.rmsnorm_bwd(inp["dy"], inp["dres"], h, inp["weight"], wl.eps)
+
+
+def oracle_sample_inputs(wl, rows):
+    from rmsnorm_fwd_bwd_03_gb300.workload import make_inputs, scaled
+    small = scaled(wl, rows, "_sample")
+    inp = make_inputs(small, "cpu", seed=0)
+    out = {}
+    for k, v in inp.items():
+        if k == "cu_seqlens":
+            out[k] = v.numpy().astype(np.int64)
+        else:
+            out[k] = v.float().numpy().astype(np.float64)
+    return small, out
+
+
+def time_oracle(wl, rows, budget_s):
+    small, inp = oracle_sample_inputs(wl, rows)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(small, inp)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": n * rows / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} passes of all 8 operators over the first {rows} tokens of {wl.name} "
+                      f"(same widths), float64 numpy, single thread, {el:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value, world):
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gbln", "reference"], default="gbln")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from rmsnorm_fwd_bwd_03_gb300.workload import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+
+    config = {"workload": wl.name, "description": wl.description, "tokens": wl.T, "hidden": wl.H,
+              "heads_q": wl.Hq, "heads_kv": wl.Hk, "head_dim": wl.D, "intermediate": wl.I,
+              "rope_theta": wl.theta, "eps": wl.eps, "fused_residual": wl.residual,
+              "global_batch_tokens": wl.T * world, "parallelism": f"replicas x{world}",
+              "l2": "flushed between timed steps (write of 2x L2 size)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        rows = 256
+        small, inp = oracle_sample_inputs(wl, rows)
+        for _ in range(args.warmup):
+            oracle_step(small, inp)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_step(small, inp)
+        el = time.perf_counter() - t0
+        value = args.steps * rows / el
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "impl": "reference", "config": config,
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                 "sample": f"each step: all 8 operators over {rows} tokens of {wl.name} "
+                                           "(same widths), float64 numpy, single thread"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from rmsnorm_fwd_bwd_03_gb300._build import build_library
+    build_library()
+
+    step = Step(wl, device, seed=rank)
+    stream = torch.cuda.current_stream(device)
+    calls = step.calls(stream.cuda_stream)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+
+    nk = len(calls)
+    for _ in range(args.warmup):
+        flush.zero_()
+        run_calls(calls)
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()
+            run_calls(calls, evs[k])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+
+    per_op = {name: 0.0 for name, _, _ in calls}
+    step_ms = []
+    for k in range(args.steps):
+        e = evs[k]
+        step_ms.append(e[0].elapsed_time(e[nk]))
+        for j, (name, _, _) in enumerate(calls):
+            per_op[name] += e[j].elapsed_time(e[j + 1])
+    total_ms = sum(step_ms)
+    total_ms_max = reduce_max(total_ms, world)
+    ms_per_step = total_ms_max / args.steps
+    value = world * wl.T * args.steps / (total_ms_max * 1e-3)
+
+    alg = wl.algorithmic_bytes()
+    peak, peak_kind = _measured_peak()
+    kernels = {}
+    for name in per_op:
+        ms = per_op[name] / args.steps
+        gbs = alg[name] / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
+        kernels[name] = {"ms": round(ms, 5), "alg_bytes": alg[name], "GB/s": round(gbs, 1),
+                         "frac_of_peak": round(gbs / peak, 4)}
+    dom = max(per_op, key=per_op.get)
+    dom_ms = per_op[dom] / args.steps
+    achieved = alg[dom] / (dom_ms * 1e-3) / 1e9
+    tr = NCU_TRAFFIC.get((wl.name, dom))
+    traffic = tr["bytes"] if tr and tr.get("src_sha") == _src_sha(dom) else None
+    step_bytes = sum(alg.values())
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "peak_kind": f"of {peak_kind}", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic, "alg_bytes_per_launch": alg[dom],
+                "frac_of_8TBps": round(achieved / 8000.0, 4)}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+            "config": config,
+            "achieved_hbm_gbs_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
+            "frac_of_peak_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4),
+            "roofline": roofline, "kernels": kernels,
+            "gpu_launches": nk * args.steps,
+            "wall_s_timed_region": round(t_wall, 3),
+            "clocks": clk.summary()}
+
+    if not args.no_e2e:
+        ins, outs = step.host_io()
+        h2d = sum(v.numel() * v.element_size() for v in ins.values())
+        d2h = sum(v.numel() * v.element_size() for v in outs.values())
+        dev_in = step.inp
+        ksteps = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            for key, hv in ins.items():
+                dev_in[key].copy_(hv, non_blocking=True)
+            run_calls(calls)
+            for key, hv in outs.items():
+                hv.copy_(step.out[key], non_blocking=True)
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(ksteps):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+        line["e2e"] = {"value": world * wl.T * ksteps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ksteps,
+                       "ms_per_step": e2e_ms / ksteps}
+        line["gpu_launches_e2e"] = nk * ksteps
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(wl, 256, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+/*
+ * gbln.h -- C ABI of the GB300 (sm_103a) layer-operator library libgbln.so.
+ *
+ * Operators: RMSNorm with fused residual add (forward, backward, weight-gradient
+ * finalize), rotary position embedding on Q and K (forward, backward, cos/sin
+ * table, per-document positions) and SwiGLU (forward, backward).
+ *
+ * Sources that name these operators (they print no formulas; the standard
+ * definitions are used and written out at each entry point):
+ *   [FL]  "Fast-LLM: 高效大语言模型训练框架", §三 技术架构: table "Transformer Block
+ *         结构" (Normalization LayerNorm / RMSNorm; attention + RoPE; MLP gated or
+ *         not, SiLU / GeLU / ReLU) and "训练配置示例" (rms_norm with epsilon;
+ *         rotary type default with theta; gated MLP with activation silu;
+ *         micro_batch_size in tokens with maximum_document_length).
+ *   [LF]  "LLaMA-Factory Kernels 系统": the fused RMSNorm, SwiGLU and RoPE operators.
+ *   [HF]  "Kernels（自定义内核）", §Liger: RMSNorm, RoPE and SwiGLU fused into single
+ *         kernels for training; fusion saves memory traffic and launches.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Memory: every pointer is DEVICE memory on the current CUDA device, owned and
+ *    allocated by the caller.  The library never allocates, never frees and keeps
+ *    no state between calls other than a per-device cache of the SM count.
+ *  - Layout: row-major and contiguous.  "[T, H]" means T rows of H elements.
+ *  - Streams: work is enqueued on `stream` (NULL = the legacy default stream) and
+ *    the call returns without synchronising.  Errors raised by the kernels
+ *    themselves appear on the stream, not in the returned status.
+ *  - Types: `io` is the element type of activations and gradients, `wt` the type
+ *    of the RMSNorm weight.  Supported: io = wt = F32; io = wt = BF16;
+ *    io = BF16 with wt = F32.  Arithmetic is float32; bf16 results are rounded
+ *    to nearest even once.
+ *  - Alignment: any alignment is accepted.  Pointers aligned to 16 bytes with
+ *    row widths that are a multiple of 16 bytes take the 128-bit vector path;
+ *    anything else takes a slower element-wise path of the same kernels.
+ *  - Errors: arguments are checked on the host before any CUDA call.  A null
+ *    required pointer, a negative or out-of-range size, eps < 0 or not finite,
+ *    an odd head size, theta <= 0, or a workspace that is too small returns an
+ *    error and launches nothing.  T == 0 (or zero elements) returns GBLN_OK and
+ *    launches nothing.  A failed launch returns GBLN_ERR_CUDA.
+ *  - Aliasing: outputs may alias their own input exactly where an entry point
+ *    says so; partial overlap is undefined.
+ */
+#ifndef GBLN_H
+#define GBLN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; declared here so that no CUDA header is needed. */
+typedef struct CUstream_st* gbln_stream_t;
+
+typedef enum {
+  GBLN_OK = 0,
+  GBLN_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad scalar                */
+  GBLN_ERR_UNSUPPORTED = 2, /* dtype combination outside the supported set       */
+  GBLN_ERR_WORKSPACE = 3,   /* dW partial workspace smaller than required        */
+  GBLN_ERR_CUDA = 4         /* a CUDA runtime call or launch failed              */
+} gbln_status;
+
+typedef enum { GBLN_F32 = 0, GBLN_BF16 = 1 } gbln_dtype;
+
+/* Human-readable name of a status code.  Never NULL; the string is static. */
+const char* gbln_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gbln_version(void);
+
+/* ------------------------------------------------------------------------- */
+/* RMSNorm with fused residual add ([FL] Transformer Block 结构, 训练配置示例;  */
+/* [LF] fused RMSNorm; [HF] §Liger)                                          */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Forward, per row t of T rows of H channels:
+ *   h[t]    = x[t] + residual[t]           (rounded to io; h = x when residual is NULL)
+ *   rstd[t] = 1 / sqrt(mean_j h[t,j]^2 + eps)
+ *   y[t,j]  = weight[j] * h[t,j] * rstd[t]  (one rounding to io)
+ *
+ * x, residual      [T, H] io, read.  residual may be NULL (plain RMSNorm).
+ * weight           [H] wt, read.
+ * y                [T, H] io, written.
+ * residual_out     [T, H] io, written with h.  Required iff residual != NULL,
+ *                  ignored otherwise.  May alias x or residual exactly.
+ * rstd             [T] float32, written; the backward pass reads it.
+ * eps              >= 0 and finite.
+ * Errors: INVALID_ARG for null x/weight/y/rstd, T < 0, H <= 0, H > 2^24, bad eps,
+ *         missing residual_out; UNSUPPORTED for other dtype pairs.
+ */
+gbln_status gbln_rmsnorm_fwd(const void* x, const void* residual, const void* weight,
+                             void* y, void* residual_out, float* rstd,
+                             int64_t T, int64_t H, float eps,
+                             gbln_dtype io, gbln_dtype wt, gbln_stream_t stream);
+
+/*
+ * Rows of the float32 weight-gradient workspace that gbln_rmsnorm_bwd writes
+ * for this shape on the current device: the workspace is [P, H] float32.
+ * P depends only on (T, H, io) and the device's SM count, so a fixed shape on a
+ * fixed GPU model always uses the same P and the same summation order.
+ * Returns P >= 1 for T >= 1, 0 for T == 0, and -1 on invalid arguments or when
+ * the device cannot be queried.
+ */
+int64_t gbln_rmsnorm_bwd_num_partials(int64_t T, int64_t H, gbln_dtype io);
+
+/*
+ * Backward, first of two passes.  With n = h * rstd and g = dy * weight, per row:
+ *   dx[t]  = rstd[t] * (g - n * mean_j(g[j] * n[j])) + dresidual_out[t]
+ *   partial[p, j] = sum over the rows of block p of dy[t,j] * n[t,j]
+ * dx is the gradient of both x and residual of the forward call.
+ *
+ * dy               [T, H] io, gradient of y.
+ * dresidual_out    [T, H] io, gradient arriving on residual_out; NULL = zero.
+ * h                [T, H] io, the forward's residual_out (or x if it had no residual).
+ * weight           [H] wt.   rstd [T] float32 from the forward.
+ * dx               [T, H] io, written.  May alias dy or dresidual_out exactly.
+ * dw_partial       [P_cap, H] float32 workspace, rows 0..P-1 written, where
+ *                  P = gbln_rmsnorm_bwd_num_partials(T, H, io).
+ * P_cap            rows available in dw_partial; GBLN_ERR_WORKSPACE if P_cap < P.
+ * The rows of a block and their order are fixed by (T, H, io, SM count): the
+ * result is bitwise reproducible run to run.
+ */
+gbln_status gbln_rmsnorm_bwd(const void* dy, const void* dresidual_out, const void* h,
+                             const void* weight, const float* rstd,
+                             void* dx, float* dw_partial, int64_t P_cap,
+                             int64_t T, int64_t H,
+                             gbln_dtype io, gbln_dtype wt, gbln_stream_t stream);
+
+/*
+ * Backward, second pass: dw[j] = (accumulate ? dw[j] : 0) + sum_{p<P} partial[p, j],
+ * summed in a fixed order (bitwise reproducible).
+ * dw_partial [P, H] float32 as written by gbln_rmsnorm_bwd, P exactly the value
+ * gbln_rmsnorm_bwd_num_partials returned for that call.  dw [H] float32.
+ */
+gbln_status gbln_rmsnorm_dw_finalize(const float* dw_partial, int64_t P, int64_t H,
+                                     float* dw, int accumulate, gbln_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Rotary position embedding on Q and K ([FL] attention with RoPE, rotary     */
+/* type default with theta; [LF] fused RoPE; [HF] §Liger)                     */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Cos/sin table: cos_sin[p, i] = (cos(p * f_i), sin(p * f_i)) as two float32,
+ * f_i = theta^(-2 i / D), for p in [0, max_pos) and i in [0, D/2).  Angles and
+ * their cosines are evaluated in double precision on the device and rounded once
+ * to float32.  cos_sin: [max_pos, D/2, 2] float32, written.
+ * Errors: INVALID_ARG for null, max_pos < 0, D <= 0 or odd, theta <= 0 or not finite.
+ */
+gbln_status gbln_rope_table(float* cos_sin, int64_t max_pos, int32_t D, double theta,
+                            gbln_stream_t stream);
+
+/*
+ * Forward rotation, rotate-half pairing.  For every token t, every head of q and
+ * of k, and i < D/2, with (c, s) = cos_sin[positions[t], i]:
+ *   out[i]       = x[i] * c - x[i + D/2] * s
+ *   out[i + D/2] = x[i + D/2] * c + x[i] * s
+ * q [T, Hq, D], k [T, Hk, D] io, read; q_out, k_out same shapes, written (may
+ * alias q and k exactly: in place).  Hk may be 0 (k, k_out ignored).
+ * positions [T] int32: the position of each token inside its document.  A position
+ * outside [0, max_pos) is not read from the table: that token's outputs are NaN.
+ * cos_sin as written by gbln_rope_table for the same D and some max_pos.
+ */
+gbln_status gbln_rope_fwd(const void* q, const void* k, void* q_out, void* k_out,
+                          const int32_t* positions, const float* cos_sin, int64_t max_pos,
+                          int64_t T, int32_t Hq, int32_t Hk, int32_t D,
+                          gbln_dtype io, gbln_stream_t stream);
+
+/*
+ * Backward: the transpose (= inverse) rotation applied to the incoming gradients:
+ *   din[i]       = dout[i] * c + dout[i + D/2] * s
+ *   din[i + D/2] = dout[i + D/2] * c - dout[i] * s
+ * Same arguments as gbln_rope_fwd with (dq, dk) in and (dq_in, dk_in) out.
+ */
+gbln_status gbln_rope_bwd(const void* dq, const void* dk, void* dq_in, void* dk_in,
+                          const int32_t* positions, const float* cos_sin, int64_t max_pos,
+                          int64_t T, int32_t Hq, int32_t Hk, int32_t D,
+                          gbln_dtype io, gbln_stream_t stream);
+
+/*
+ * Positions of packed documents: positions[t] = t - cu_seqlens[d] for the document
+ * d with cu_seqlens[d] <= t < cu_seqlens[d+1] ([FL] 训练配置示例: micro-batches
+ * counted in tokens hold several documents of at most maximum_document_length).
+ * cu_seqlens [ndoc + 1] int32, non-decreasing, cu_seqlens[0] = 0 and
+ * cu_seqlens[ndoc] = T (caller's contract: violating it gives wrong but in-bounds
+ * results).  positions [T] int32, written.
+ */
+gbln_status gbln_positions_from_cu_seqlens(const int32_t* cu_seqlens, int32_t ndoc,
+                                           int32_t* positions, int64_t T,
+                                           gbln_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* SwiGLU ([FL] 支持的 MLP 变体, 训练配置示例 gated + silu; [LF] fused SwiGLU;   */
+/* [HF] §Liger)                                                              */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * out = silu(gate) * up = gate / (1 + exp(-gate)) * up, elementwise.
+ * gate, up, out: [T, I] io.  out may alias gate or up exactly.
+ */
+gbln_status gbln_swiglu_fwd(const void* gate, const void* up, void* out,
+                            int64_t T, int64_t I, gbln_dtype io, gbln_stream_t stream);
+
+/*
+ * With s = sigmoid(gate):
+ *   dgate = dout * up * s * (1 + gate * (1 - s))
+ *   dup   = dout * gate * s
+ * dout, gate, up: [T, I] io, read.  dgate, dup: [T, I] io, written; dgate may
+ * alias gate and dup may alias up exactly (in place).
+ */
+gbln_status gbln_swiglu_bwd(const void* dout, const void* gate, const void* up,
+                            void* dgate, void* dup,
+                            int64_t T, int64_t I, gbln_dtype io, gbln_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBLN_H */

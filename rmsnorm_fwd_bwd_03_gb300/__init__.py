@@ -1,0 +1,277 @@
+"""Thin Python binding of libgbln (RMSNorm / RoPE / SwiGLU, forward and backward, sm_103a).
+
+Each function here marshals torch tensors into the C ABI declared in
+``include/gbln.h`` and calls the entry point of the same name (``rmsnorm_fwd`` ->
+``gbln_rmsnorm_fwd`` and so on) on the tensor's current CUDA stream.  Outputs that
+are not passed in are allocated with torch (device memory is torch's job); every
+step of the computation runs in the library's CUDA kernels.  There is no CPU
+path: without the built library every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB as _LIB_PATH
+
+__all__ = [
+    "GblnError", "library", "library_path", "status_string", "version",
+    "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_num_partials", "rmsnorm_dw_finalize",
+    "rope_table", "rope_fwd", "rope_bwd", "positions_from_cu_seqlens",
+    "swiglu_fwd", "swiglu_bwd",
+    "F32", "BF16",
+]
+
+F32 = 0
+BF16 = 1
+_DTYPE = {torch.float32: F32, torch.bfloat16: BF16}
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_f32 = ctypes.c_float
+_f64 = ctypes.c_double
+
+# name -> (restype, argtypes); mirrors include/gbln.h
+_SIGNATURES = {
+    "gbln_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "gbln_version": (ctypes.c_int, []),
+    "gbln_rmsnorm_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, ctypes.c_int, ctypes.c_int, _vp]),
+    "gbln_rmsnorm_bwd_num_partials": (_i64, [_i64, _i64, ctypes.c_int]),
+    "gbln_rmsnorm_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
+    "gbln_rmsnorm_dw_finalize": (ctypes.c_int, [_vp, _i64, _i64, _vp, ctypes.c_int, _vp]),
+    "gbln_rope_table": (ctypes.c_int, [_vp, _i64, _i32, _f64, _vp]),
+    "gbln_rope_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, ctypes.c_int, _vp]),
+    "gbln_rope_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, ctypes.c_int, _vp]),
+    "gbln_positions_from_cu_seqlens": (ctypes.c_int, [_vp, _i32, _vp, _i64, _vp]),
+    "gbln_swiglu_fwd": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp]),
+    "gbln_swiglu_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp]),
+}
+
+_lib = None
+
+
+class GblnError(RuntimeError):
+    """A libgbln entry point returned a non-zero status."""
+
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def library():
+    """Load libgbln.so (built by ``__graft_entry__.build()``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"libgbln.so not found at {_LIB_PATH}: build it with __graft_entry__.build() "
+            "(there is no fallback implementation)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return library().gbln_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return library().gbln_version()
+
+
+def _check(fn, status):
+    if status != 0:
+        raise GblnError(fn, status)
+
+
+def _io(t: torch.Tensor) -> int:
+    try:
+        return _DTYPE[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}; expected float32 or bfloat16") from None
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
+    return t.data_ptr()
+
+
+def _opt(t, name):
+    return None if t is None else _dev(t, name)
+
+
+def _stream(t: torch.Tensor):
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm
+# ---------------------------------------------------------------------------
+
+def rmsnorm_fwd(x, weight, eps, residual=None, *, y=None, residual_out=None, rstd=None):
+    """``gbln_rmsnorm_fwd``.  x, residual: [T, H]; weight: [H].  Returns ``(y, h, rstd)``.
+
+    h is ``x + residual`` rounded to x's dtype (``residual_out``), or x itself when
+    residual is None; rstd is float32 [T].
+    """
+    H = x.shape[-1]
+    T = x.numel() // H if H else 0
+    if y is None:
+        y = torch.empty_like(x)
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(x)
+    if rstd is None:
+        rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    st = library().gbln_rmsnorm_fwd(
+        _dev(x, "x"), _opt(residual, "residual"), _dev(weight, "weight"), _dev(y, "y"),
+        _opt(residual_out, "residual_out") if residual is not None else None, _dev(rstd, "rstd"),
+        T, H, float(eps), _io(x), _io(weight), _stream(x))
+    _check("gbln_rmsnorm_fwd", st)
+    return y, (residual_out if residual is not None else x), rstd
+
+
+def rmsnorm_bwd_num_partials(T: int, H: int, dtype=torch.bfloat16) -> int:
+    """``gbln_rmsnorm_bwd_num_partials``: rows P of the [P, H] float32 dW workspace."""
+    P = library().gbln_rmsnorm_bwd_num_partials(int(T), int(H), _DTYPE[dtype])
+    if P < 0:
+        raise GblnError("gbln_rmsnorm_bwd_num_partials", 1)
+    return int(P)
+
+
+def rmsnorm_bwd(dy, h, weight, rstd, dresidual_out=None, *, dx=None, dw_partial=None):
+    """``gbln_rmsnorm_bwd``.  Returns ``(dx, dw_partial, P)``; finish dW with :func:`rmsnorm_dw_finalize`."""
+    H = dy.shape[-1]
+    T = dy.numel() // H if H else 0
+    P = rmsnorm_bwd_num_partials(T, H, dy.dtype)
+    if dx is None:
+        dx = torch.empty_like(dy)
+    if dw_partial is None:
+        dw_partial = torch.empty((max(P, 1), H), dtype=torch.float32, device=dy.device)
+    st = library().gbln_rmsnorm_bwd(
+        _dev(dy, "dy"), _opt(dresidual_out, "dresidual_out"), _dev(h, "h"), _dev(weight, "weight"),
+        _dev(rstd, "rstd"), _dev(dx, "dx"), _dev(dw_partial, "dw_partial"), dw_partial.shape[0],
+        T, H, _io(dy), _io(weight), _stream(dy))
+    _check("gbln_rmsnorm_bwd", st)
+    return dx, dw_partial, P
+
+
+def rmsnorm_dw_finalize(dw_partial, P, dw=None, accumulate=False):
+    """``gbln_rmsnorm_dw_finalize``: float32 dW [H] = fixed-order sum of the first P partial rows."""
+    H = dw_partial.shape[-1]
+    if dw is None:
+        dw = torch.empty(H, dtype=torch.float32, device=dw_partial.device)
+    st = library().gbln_rmsnorm_dw_finalize(
+        _dev(dw_partial, "dw_partial"), int(P), H, _dev(dw, "dw"), 1 if accumulate else 0,
+        _stream(dw_partial))
+    _check("gbln_rmsnorm_dw_finalize", st)
+    return dw
+
+
+# ---------------------------------------------------------------------------
+# RoPE
+# ---------------------------------------------------------------------------
+
+def rope_table(max_pos: int, D: int, theta: float, device=None, out=None):
+    """``gbln_rope_table``: float32 [max_pos, D/2, 2] of (cos, sin)(p * theta^(-2i/D))."""
+    if out is None:
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        out = torch.empty((max_pos, D // 2, 2), dtype=torch.float32, device=dev)
+    st = library().gbln_rope_table(_dev(out, "cos_sin"), int(max_pos), int(D), float(theta), _stream(out))
+    _check("gbln_rope_table", st)
+    return out
+
+
+def _rope(name, q, k, positions, cos_sin, q_out, k_out):
+    T, Hq, D = q.shape
+    Hk = 0 if k is None else k.shape[1]
+    if k is not None and (k.shape[0] != T or k.shape[2] != D or k.dtype != q.dtype):
+        raise ValueError("k must be [T, Hk, D] with q's T, D and dtype")
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    if k is not None and k_out is None:
+        k_out = torch.empty_like(k)
+    st = getattr(library(), name)(
+        _dev(q, "q"), _opt(k, "k"), _dev(q_out, "q_out"), _opt(k_out, "k_out"),
+        _dev(positions, "positions"), _dev(cos_sin, "cos_sin"), cos_sin.shape[0],
+        T, Hq, Hk, D, _io(q), _stream(q))
+    _check(name, st)
+    return q_out, k_out
+
+
+def rope_fwd(q, k, positions, cos_sin, *, q_out=None, k_out=None):
+    """``gbln_rope_fwd``: rotate q [T, Hq, D] and k [T, Hk, D] by positions [T] (int32).
+
+    Pass ``q_out=q, k_out=k`` to rotate in place.  Returns ``(q_out, k_out)``.
+    """
+    return _rope("gbln_rope_fwd", q, k, positions, cos_sin, q_out, k_out)
+
+
+def rope_bwd(dq, dk, positions, cos_sin, *, dq_in=None, dk_in=None):
+    """``gbln_rope_bwd``: inverse rotation of the gradients.  Returns ``(dq_in, dk_in)``."""
+    return _rope("gbln_rope_bwd", dq, dk, positions, cos_sin, dq_in, dk_in)
+
+
+def positions_from_cu_seqlens(cu_seqlens, T: int, out=None):
+    """``gbln_positions_from_cu_seqlens``: int32 [T] position of each token in its document."""
+    if cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if out is None:
+        out = torch.empty(T, dtype=torch.int32, device=cu_seqlens.device)
+    st = library().gbln_positions_from_cu_seqlens(
+        _dev(cu_seqlens, "cu_seqlens"), cu_seqlens.numel() - 1, _dev(out, "positions"), int(T),
+        _stream(cu_seqlens))
+    _check("gbln_positions_from_cu_seqlens", st)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU
+# ---------------------------------------------------------------------------
+
+def swiglu_fwd(gate, up, out=None):
+    """``gbln_swiglu_fwd``: silu(gate) * up for [T, I] tensors."""
+    if gate.shape != up.shape or gate.dtype != up.dtype:
+        raise ValueError("gate and up must have the same shape and dtype")
+    I = gate.shape[-1]
+    T = gate.numel() // I if I else 0
+    if out is None:
+        out = torch.empty_like(gate)
+    st = library().gbln_swiglu_fwd(_dev(gate, "gate"), _dev(up, "up"), _dev(out, "out"), T, I,
+                                   _io(gate), _stream(gate))
+    _check("gbln_swiglu_fwd", st)
+    return out
+
+
+def swiglu_bwd(dout, gate, up, dgate=None, dup=None):
+    """``gbln_swiglu_bwd``.  Returns ``(dgate, dup)``."""
+    if not (dout.shape == gate.shape == up.shape) or not (dout.dtype == gate.dtype == up.dtype):
+        raise ValueError("dout, gate and up must have the same shape and dtype")
+    I = gate.shape[-1]
+    T = gate.numel() // I if I else 0
+    if dgate is None:
+        dgate = torch.empty_like(gate)
+    if dup is None:
+        dup = torch.empty_like(up)
+    st = library().gbln_swiglu_bwd(_dev(dout, "dout"), _dev(gate, "gate"), _dev(up, "up"),
+                                   _dev(dgate, "dgate"), _dev(dup, "dup"), T, I, _io(gate),
+                                   _stream(gate))
+    _check("gbln_swiglu_bwd", st)
+    return dgate, dup

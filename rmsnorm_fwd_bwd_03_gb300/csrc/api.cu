@@ -1,0 +1,45 @@
+// Library-wide entry points of libgbln: status strings, version, and the
+// per-device SM-count cache used to size persistent grids.
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace gbln {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];  // 0 = not yet queried
+}  // namespace
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return -1;
+  int v = g_sms[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+    cudaGetLastError();
+    return -1;
+  }
+  g_sms[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+}  // namespace gbln
+
+extern "C" const char* gbln_status_string(int status) {
+  switch (status) {
+    case GBLN_OK: return "GBLN_OK";
+    case GBLN_ERR_INVALID_ARG: return "GBLN_ERR_INVALID_ARG: invalid argument";
+    case GBLN_ERR_UNSUPPORTED: return "GBLN_ERR_UNSUPPORTED: unsupported dtype combination";
+    case GBLN_ERR_WORKSPACE: return "GBLN_ERR_WORKSPACE: dW partial workspace too small";
+    case GBLN_ERR_CUDA: return "GBLN_ERR_CUDA: CUDA launch or runtime call failed";
+    default: return "unknown gbln status";
+  }
+}
+
+extern "C" int gbln_version(void) { return 100; }

@@ -1,0 +1,134 @@
+// Shared device helpers of libgbln: 128-bit packs of bf16 / f32, fp32 row
+// reductions and host-side argument checks.  Nothing here is used by the CPU
+// oracle, and nothing from it is used here.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "gbln.h"
+
+namespace gbln {
+
+typedef __nv_bfloat16 bf16;
+
+// Elements per 16-byte access.
+template <typename T> struct VecOf;
+template <> struct VecOf<float> { static constexpr int N = 4; };
+template <> struct VecOf<bf16> { static constexpr int N = 8; };
+
+// ---------------------------------------------------------------------------
+// Loads and stores of N consecutive elements as float32.
+// N * sizeof(T) == 16 uses one 128-bit access (pointer must be 16-B aligned);
+// N == 1 is the element-wise path for unaligned rows.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // round to nearest even
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(bf16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// Streaming read of data touched once: no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+// Read-only data reused across rows (weights, cos/sin table): cached path.
+__device__ __forceinline__ uint4 ld_reuse(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void st_vec(void* p, uint4 v) {
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+template <int N> __device__ __forceinline__ void unpack(uint4 a, float (&v)[N]);
+template <> __device__ __forceinline__ void unpack<4>(uint4 a, float (&v)[4]) {
+  v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+  v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+}
+template <> __device__ __forceinline__ void unpack<8>(uint4 a, float (&v)[8]) {
+  v[0] = bf16_lo(a.x); v[1] = bf16_hi(a.x); v[2] = bf16_lo(a.y); v[3] = bf16_hi(a.y);
+  v[4] = bf16_lo(a.z); v[5] = bf16_hi(a.z); v[6] = bf16_lo(a.w); v[7] = bf16_hi(a.w);
+}
+
+template <typename T, int N> __device__ __forceinline__ uint4 pack(const float (&v)[N]);
+template <> __device__ __forceinline__ uint4 pack<float, 4>(const float (&v)[4]) {
+  return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                    __float_as_uint(v[3]));
+}
+template <> __device__ __forceinline__ uint4 pack<bf16, 8>(const float (&v)[8]) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+
+// Generic N-element load/store: one 128-bit access when N fills 16 bytes, else scalars.
+template <typename T, int N, bool STREAM = true>
+__device__ __forceinline__ void load_n(const T* p, float (&v)[N]) {
+  if constexpr (N * sizeof(T) == 16) {
+    unpack<N>(STREAM ? ld_stream(p) : ld_reuse(p), v);
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e) v[e] = to_f32(p[e]);
+  }
+}
+template <typename T, int N>
+__device__ __forceinline__ void store_n(T* p, const float (&v)[N]) {
+  if constexpr (N * sizeof(T) == 16) {
+    st_vec(p, pack<T, N>(v));
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e) p[e] = from_f32<T>(v[e]);
+  }
+}
+// Round float32 values to T and back (what a store followed by a load would see).
+template <typename T, int N>
+__device__ __forceinline__ void round_to(float (&v)[N]) {
+  if constexpr (sizeof(T) == 2) {
+#pragma unroll
+    for (int e = 0; e < N; ++e) v[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
+  }
+}
+
+// Sum over groups of W consecutive lanes (W a power of two <= 32); every lane
+// of the group gets the total.  The butterfly order is fixed: deterministic.
+template <int W>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = W / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o, W);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+int sm_count();  // SM count of the current device (cached per device); <= 0 on failure
+
+inline size_t dtype_size(gbln_dtype t) { return t == GBLN_BF16 ? 2 : 4; }
+inline bool dtype_ok(int t) { return t == GBLN_F32 || t == GBLN_BF16; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline gbln_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? GBLN_OK : GBLN_ERR_CUDA;
+}
+
+inline unsigned grid_for(int64_t work, int block, int64_t cap) {
+  int64_t g = (work + block - 1) / block;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return (unsigned)g;
+}
+
+}  // namespace gbln

@@ -1,0 +1,95 @@
+"""Tolerances and sampling shared by the GPU parity tests.
+
+Bounds (written here, used everywhere):
+  * float32 I/O: normwise maximum relative error  max|gpu - ref| / max|ref| <= 1e-5
+    (elementwise relative error is ill-posed where outputs cross zero);
+  * bf16 I/O: elementwise |gpu - ref| <= 1e-2 * |ref| + 1e-3, against the float64
+    oracle value before any rounding to bf16;
+  * RMSNorm weight gradient (float32 [H]): ||gpu - ref||_2 / ||ref||_2 <= 1e-3;
+  * the residual-stream output h and integer positions: bit-exact;
+  * rstd (float32 in both I/O types): elementwise relative 1e-5.
+"""
+
+import numpy as np
+import torch
+
+F32_NORMWISE = 1e-5
+BF16_REL = 1e-2
+BF16_ABS = 1e-3
+DW_REL_L2 = 1e-3
+RSTD_REL = 1e-5
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    """Exact float64 copy of a float32 / bf16 tensor (any device)."""
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def check_io(got, ref, io: str, what: str):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    if got.size == 0:
+        return
+    if io == "f32":
+        scale = np.max(np.abs(ref))
+        err = np.max(np.abs(got - ref)) / (scale if scale > 0 else 1.0)
+        assert err <= F32_NORMWISE, f"{what}: normwise max rel err {err:.3e} > {F32_NORMWISE}"
+    else:
+        err = np.abs(got - ref)
+        bound = BF16_REL * np.abs(ref) + BF16_ABS
+        bad = err > bound
+        if bad.any():
+            i = np.unravel_index(np.argmax(err - bound), err.shape)
+            raise AssertionError(
+                f"{what}: {int(bad.sum())} of {err.size} elements out of bound; worst at {i}: "
+                f"got {got[i]!r} ref {ref[i]!r}")
+
+
+def check_dw(got, ref, what="dW"):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel <= DW_REL_L2, f"{what}: rel-L2 {rel:.3e} > {DW_REL_L2}"
+
+
+def check_rstd(got, ref, what="rstd"):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rel = np.max(np.abs(got - ref) / np.abs(ref)) if ref.size else 0.0
+    assert rel <= RSTD_REL, f"{what}: max rel err {rel:.3e} > {RSTD_REL}"
+
+
+def sample_rows(T: int, n: int, seed: int = 123, extra=()) -> np.ndarray:
+    """Seeded sample of row indices plus the first and last rows and any `extra` rows."""
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(T, size=min(n, T), replace=False).tolist()) if T else set()
+    rows.update(int(r) for r in extra if 0 <= r < T)
+    if T:
+        rows.update([0, T - 1])
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+class Guarded:
+    """A CUDA buffer with canary bands before and after the usable region."""
+
+    BAND = 4096  # bytes on each side
+
+    def __init__(self, shape, dtype, device="cuda", fill=0xA5):
+        n = int(np.prod(shape)) if len(shape) else 1
+        esz = torch.empty((), dtype=dtype).element_size()
+        band = self.BAND // esz
+        self.raw = torch.empty(n + 2 * band, dtype=dtype, device=device)
+        self.raw.view(torch.uint8).fill_(fill)
+        self.band = band
+        self.n = n
+        self.fill = fill
+        self.tensor = self.raw[band:band + n].view(shape)
+
+    def intact(self) -> bool:
+        b = self.raw.view(torch.uint8)
+        esz = self.raw.element_size()
+        head = b[: self.band * esz]
+        tail = b[(self.band + self.n) * esz:]
+        return bool((head == self.fill).all()) and bool((tail == self.fill).all())

@@ -1,0 +1,146 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads and
+exports every entry point declared in include/gbln.h, and every invalid argument
+is rejected on the host with the documented status before any CUDA call (these
+calls never reach the device, so they run without one)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+F32, BF16 = 0, 1
+FAKE = 0x10000  # never dereferenced: every call below returns before touching memory
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rmsnorm_fwd_bwd_03_gb300._build import build_library
+    import rmsnorm_fwd_bwd_03_gb300 as gb
+    build_library()
+    return gb.library()
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            with open(os.path.join(ROOT, "include", f), encoding="utf-8") as fh:
+                src = fh.read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names.update(re.findall(r"\b(gbln_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 12
+    for n in sorted(names):
+        assert hasattr(lib, n), f"{n} declared but not exported"
+    raw = ctypes.CDLL(lib._name)
+    for n in names:
+        getattr(raw, n)
+
+
+def test_status_strings_and_version(lib):
+    for s in range(5):
+        assert lib.gbln_status_string(s).decode().startswith("GBLN_")
+    assert b"unknown" in lib.gbln_status_string(99)
+    assert lib.gbln_version() >= 100
+
+
+def _fwd(lib, x=FAKE, r=None, w=FAKE, y=FAKE, ho=None, rstd=FAKE, T=4, H=8, eps=1e-5, io=BF16, wt=BF16):
+    return lib.gbln_rmsnorm_fwd(x, r, w, y, ho, rstd, T, H, eps, io, wt, None)
+
+
+def test_rmsnorm_fwd_rejects(lib):
+    assert _fwd(lib, x=None) == INVALID
+    assert _fwd(lib, w=None) == INVALID
+    assert _fwd(lib, y=None) == INVALID
+    assert _fwd(lib, rstd=None) == INVALID
+    assert _fwd(lib, r=FAKE, ho=None) == INVALID
+    assert _fwd(lib, T=-1) == INVALID
+    assert _fwd(lib, H=0) == INVALID
+    assert _fwd(lib, H=(1 << 24) + 1) == INVALID
+    assert _fwd(lib, eps=-1e-6) == INVALID
+    assert _fwd(lib, eps=float("nan")) == INVALID
+    assert _fwd(lib, eps=float("inf")) == INVALID
+    assert _fwd(lib, io=7) == INVALID
+    assert _fwd(lib, io=F32, wt=BF16) == UNSUPPORTED
+    assert _fwd(lib, T=0) == OK  # nothing to do, nothing launched
+    assert _fwd(lib, T=0, r=FAKE, ho=FAKE, io=BF16, wt=F32) == OK
+
+
+def test_rmsnorm_bwd_and_finalize_reject(lib):
+    def bwd(dy=FAKE, dr=None, h=FAKE, w=FAKE, rs=FAKE, dx=FAKE, part=FAKE, P=10, T=4, H=8, io=BF16, wt=BF16):
+        return lib.gbln_rmsnorm_bwd(dy, dr, h, w, rs, dx, part, P, T, H, io, wt, None)
+    for kw in ({"dy": None}, {"h": None}, {"w": None}, {"rs": None}, {"dx": None}, {"part": None},
+               {"T": -3}, {"H": 0}, {"P": -1}, {"io": 5}):
+        assert bwd(**kw) == INVALID, kw
+    assert bwd(io=F32, wt=BF16) == UNSUPPORTED
+    assert bwd(T=0) == OK
+    assert lib.gbln_rmsnorm_bwd_num_partials(-1, 8, BF16) == -1
+    assert lib.gbln_rmsnorm_bwd_num_partials(4, 0, BF16) == -1
+    assert lib.gbln_rmsnorm_bwd_num_partials(4, 8, 9) == -1
+    assert lib.gbln_rmsnorm_bwd_num_partials(0, 8, BF16) == 0
+    assert lib.gbln_rmsnorm_dw_finalize(FAKE, -1, 8, FAKE, 0, None) == INVALID
+    assert lib.gbln_rmsnorm_dw_finalize(FAKE, 4, 0, FAKE, 0, None) == INVALID
+    assert lib.gbln_rmsnorm_dw_finalize(FAKE, 4, 8, None, 0, None) == INVALID
+    assert lib.gbln_rmsnorm_dw_finalize(None, 4, 8, FAKE, 0, None) == INVALID
+
+
+def test_rope_rejects(lib):
+    def rope(fn, q=FAKE, k=FAKE, qo=FAKE, ko=FAKE, pos=FAKE, cs=FAKE, mp=100, T=4, Hq=2, Hk=1, D=8, io=BF16):
+        return getattr(lib, fn)(q, k, qo, ko, pos, cs, mp, T, Hq, Hk, D, io, None)
+    for fn in ("gbln_rope_fwd", "gbln_rope_bwd"):
+        for kw in ({"q": None}, {"qo": None}, {"k": None}, {"ko": None}, {"pos": None}, {"cs": None},
+                   {"D": 7}, {"D": 0}, {"Hq": 0, "Hk": 0}, {"Hq": -1}, {"T": -1}, {"mp": -1},
+                   {"cs": FAKE + 4}, {"io": 3}):
+            assert rope(fn, **kw) == INVALID, (fn, kw)
+        assert rope(fn, T=0) == OK
+        assert rope(fn, T=0, k=None, ko=None, Hk=0) == OK
+    assert lib.gbln_rope_table(None, 10, 8, 1e4, None) == INVALID
+    assert lib.gbln_rope_table(FAKE, -1, 8, 1e4, None) == INVALID
+    assert lib.gbln_rope_table(FAKE, 10, 7, 1e4, None) == INVALID
+    assert lib.gbln_rope_table(FAKE, 10, 8, 0.0, None) == INVALID
+    assert lib.gbln_rope_table(FAKE, 10, 8, float("nan"), None) == INVALID
+    assert lib.gbln_rope_table(FAKE, 0, 8, 1e4, None) == OK
+
+
+def test_positions_rejects(lib):
+    f = lib.gbln_positions_from_cu_seqlens
+    assert f(FAKE, 2, None, 10, None) == INVALID
+    assert f(FAKE, -1, FAKE, 10, None) == INVALID
+    assert f(None, 2, FAKE, 10, None) == INVALID
+    assert f(FAKE, 0, FAKE, 10, None) == INVALID
+    assert f(FAKE, 2, FAKE, -1, None) == INVALID
+    assert f(None, 0, FAKE, 0, None) == OK
+
+
+def test_swiglu_rejects(lib):
+    assert lib.gbln_swiglu_fwd(None, FAKE, FAKE, 4, 8, BF16, None) == INVALID
+    assert lib.gbln_swiglu_fwd(FAKE, None, FAKE, 4, 8, BF16, None) == INVALID
+    assert lib.gbln_swiglu_fwd(FAKE, FAKE, None, 4, 8, BF16, None) == INVALID
+    assert lib.gbln_swiglu_fwd(FAKE, FAKE, FAKE, -1, 8, BF16, None) == INVALID
+    assert lib.gbln_swiglu_fwd(FAKE, FAKE, FAKE, 4, 0, BF16, None) == INVALID
+    assert lib.gbln_swiglu_fwd(FAKE, FAKE, FAKE, 1 << 40, 1 << 30, BF16, None) == INVALID
+    assert lib.gbln_swiglu_fwd(FAKE, FAKE, FAKE, 4, 8, 2, None) == INVALID
+    assert lib.gbln_swiglu_fwd(FAKE, FAKE, FAKE, 0, 8, BF16, None) == OK
+    for i in range(5):
+        args = [FAKE] * 5
+        args[i] = None
+        assert lib.gbln_swiglu_bwd(*args, 4, 8, BF16, None) == INVALID
+    assert lib.gbln_swiglu_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 8, F32, None) == OK
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    import rmsnorm_fwd_bwd_03_gb300 as gb
+    x = torch.zeros(2, 8)
+    with pytest.raises(ValueError):
+        gb.rmsnorm_fwd(x, torch.ones(8), 1e-5)
+    with pytest.raises(ValueError):
+        gb.swiglu_fwd(x, x)
