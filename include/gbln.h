@@ -35,8 +35,9 @@
  *  - Errors: arguments are checked on the host before any CUDA call.  A null
  *    required pointer, a negative or out-of-range size, eps < 0 or not finite,
  *    an odd head size, theta <= 0, or a workspace that is too small returns an
- *    error and launches nothing.  T == 0 (or zero elements) returns GBLN_OK and
- *    launches nothing.  A failed launch returns GBLN_ERR_CUDA.
+ *    error and launches nothing.  T == 0 returns GBLN_OK and launches nothing
+ *    once sizes, scalars and dtypes pass; its pointers are not examined (empty
+ *    tensors may have null data pointers).  A failed launch returns GBLN_ERR_CUDA.
  *  - Aliasing: outputs may alias their own input exactly where an entry point
  *    says so; partial overlap is undefined.
  */

@@ -476,10 +476,10 @@ extern "C" gbln_status gbln_rmsnorm_fwd(const void* x, const void* residual, con
   if (!dtype_ok(io) || !dtype_ok(wt)) return GBLN_ERR_INVALID_ARG;
   if (T < 0 || T > kMaxRows || H <= 0 || H > kMaxH) return GBLN_ERR_INVALID_ARG;
   if (!(eps >= 0.0f && eps <= 3.4028235e38f)) return GBLN_ERR_INVALID_ARG;  // also rejects NaN
+  if (!dtypes_ok(io, wt)) return GBLN_ERR_UNSUPPORTED;
+  if (T == 0) return GBLN_OK;  // nothing is read or written: pointers are not examined
   if (!x || !weight || !y || !rstd) return GBLN_ERR_INVALID_ARG;
   if (residual && !residual_out) return GBLN_ERR_INVALID_ARG;
-  if (!dtypes_ok(io, wt)) return GBLN_ERR_UNSUPPORTED;
-  if (T == 0) return GBLN_OK;
   const void* r = residual;
   void* ho = residual ? residual_out : nullptr;
   cudaStream_t s = (cudaStream_t)stream;
@@ -502,9 +502,9 @@ extern "C" gbln_status gbln_rmsnorm_bwd(const void* dy, const void* dresidual_ou
                                         gbln_dtype io, gbln_dtype wt, gbln_stream_t stream) {
   if (!dtype_ok(io) || !dtype_ok(wt)) return GBLN_ERR_INVALID_ARG;
   if (T < 0 || T > kMaxRows || H <= 0 || H > kMaxH || P_cap < 0) return GBLN_ERR_INVALID_ARG;
-  if (!dy || !h || !weight || !rstd || !dx || !dw_partial) return GBLN_ERR_INVALID_ARG;
   if (!dtypes_ok(io, wt)) return GBLN_ERR_UNSUPPORTED;
-  if (T == 0) return GBLN_OK;
+  if (T == 0) return GBLN_OK;  // nothing is read or written: pointers are not examined
+  if (!dy || !h || !weight || !rstd || !dx || !dw_partial) return GBLN_ERR_INVALID_ARG;
   const int sms = sm_count();
   if (sms <= 0) return GBLN_ERR_CUDA;
   const int64_t P = partials_for(T, geometry(H, dtype_size(io)), sms);

@@ -8,11 +8,11 @@
 // Pairing is rotate-half: element i turns with element i + D/2.
 //
 // HBM-bound design: one thread moves the two 16-byte vectors at i and i + D/2
-// of one head row, so each element is read and written exactly once (in place
-// is allowed).  Consecutive threads cover consecutive (token, head, vector)
-// units, so all heads of a token sit in one or two neighbouring blocks and the
-// token's position and cos/sin row (float32, from a table built once in double
-// precision) are re-read from L1 / L2, not from HBM.
+// of a head row, so each element is read and written exactly once (in place is
+// allowed).  A block covers all heads of one token at a time; each thread
+// reads the token's position and its slice of the cos/sin row (float32, from a
+// table built once in double precision, served from L1 / L2) once and applies
+// it to every head it owns.  No integer division in the token loop.
 
 #include "common.cuh"
 
@@ -20,44 +20,28 @@ namespace gbln {
 
 namespace {
 
-constexpr int kRopeBlock = 256;
-
-// One thread per (token, head, vector) unit, grid-stride over the flat unit
-// index; `per_tok` = (Hq + Hk) * (D/2/VEC) units per token.
-template <typename T, int VEC, bool BWD>
-__global__ void __launch_bounds__(kRopeBlock)
+// Block of HP * NVH threads, NVH = D/2/VEC vectors per half head row: thread
+// (hl, v) owns vector v (elements v*VEC.. and D/2 + v*VEC..) of heads hl,
+// hl + HP, ... of every token the block visits; tokens are strided by gridDim.
+// The cos/sin vector of a token is loaded once per thread and reused for all
+// its heads; up to HPT heads' loads are issued before any of them is used.
+template <typename T, int VEC, bool BWD, int HPT>
+__global__ void __launch_bounds__(512)
 rope_kernel(const T* q, const T* k, T* qo, T* ko, const int32_t* __restrict__ pos,
             const float2* __restrict__ cs, int64_t max_pos, int64_t T_, int Hq, int Hk,
-            int D) {
+            int D, int HP) {
   const int half = D / 2;
   const int nvh = half / VEC;
-  const int per_tok = (Hq + Hk) * nvh;
-  const int64_t total = T_ * (int64_t)per_tok;
-  const int64_t stride = (int64_t)gridDim.x * kRopeBlock;
-  for (int64_t u = (int64_t)blockIdx.x * kRopeBlock + threadIdx.x; u < total; u += stride) {
-    const int64_t t = u / per_tok;
-    const int rem = (int)(u - t * per_tok);
-    const int hd = rem / nvh;
-    const int i0 = (rem - hd * nvh) * VEC;
-    const T* src;
-    T* dst;
-    if (hd < Hq) {
-      const size_t off = ((size_t)t * Hq + hd) * D;
-      src = q + off; dst = qo + off;
-    } else {
-      const size_t off = ((size_t)t * Hk + (hd - Hq)) * D;
-      src = k + off; dst = ko + off;
-    }
-    float a[VEC], b[VEC], o1[VEC], o2[VEC];
-    load_n<T, VEC>(src + i0, a);
-    load_n<T, VEC>(src + half + i0, b);
+  const int v = threadIdx.x % nvh;
+  const int hl = threadIdx.x / nvh;
+  const int HT = Hq + Hk;
+  const int i0 = v * VEC;
+  for (int64_t t = blockIdx.x; t < T_; t += gridDim.x) {
     const int p = __ldg(pos + t);
-    if (p < 0 || (int64_t)p >= max_pos) {
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) { o1[e] = __int_as_float(0x7fc00000); o2[e] = o1[e]; }
-    } else {
+    const bool ok = p >= 0 && (int64_t)p < max_pos;
+    float cv[VEC], sv[VEC];
+    if (ok) {
       const float2* c = cs + (size_t)p * half + i0;
-      float cv[VEC], sv[VEC];
       if constexpr (VEC % 2 == 0) {
 #pragma unroll
         for (int e = 0; e < VEC; e += 2) {
@@ -68,19 +52,42 @@ rope_kernel(const T* q, const T* k, T* qo, T* ko, const int32_t* __restrict__ po
 #pragma unroll
         for (int e = 0; e < VEC; ++e) { const float2 f = __ldg(c + e); cv[e] = f.x; sv[e] = f.y; }
       }
+    } else {  // out-of-range position: never read the table, emit NaN
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        if constexpr (!BWD) {
-          o1[e] = a[e] * cv[e] - b[e] * sv[e];
-          o2[e] = b[e] * cv[e] + a[e] * sv[e];
-        } else {
-          o1[e] = a[e] * cv[e] + b[e] * sv[e];
-          o2[e] = b[e] * cv[e] - a[e] * sv[e];
+      for (int e = 0; e < VEC; ++e) { cv[e] = __int_as_float(0x7fc00000); sv[e] = cv[e]; }
+    }
+    for (int h0 = hl; h0 < HT; h0 += HP * HPT) {
+      float a[HPT][VEC], b[HPT][VEC];
+#pragma unroll
+      for (int j = 0; j < HPT; ++j) {
+        const int h = h0 + j * HP;
+        if (h < HT) {
+          const T* src = h < Hq ? q + ((size_t)t * Hq + h) * D : k + ((size_t)t * Hk + (h - Hq)) * D;
+          load_n<T, VEC>(src + i0, a[j]);
+          load_n<T, VEC>(src + half + i0, b[j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < HPT; ++j) {
+        const int h = h0 + j * HP;
+        if (h < HT) {
+          T* dst = h < Hq ? qo + ((size_t)t * Hq + h) * D : ko + ((size_t)t * Hk + (h - Hq)) * D;
+          float o1[VEC], o2[VEC];
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            if constexpr (!BWD) {
+              o1[e] = a[j][e] * cv[e] - b[j][e] * sv[e];
+              o2[e] = b[j][e] * cv[e] + a[j][e] * sv[e];
+            } else {
+              o1[e] = a[j][e] * cv[e] + b[j][e] * sv[e];
+              o2[e] = b[j][e] * cv[e] - a[j][e] * sv[e];
+            }
+          }
+          store_n<T, VEC>(dst + i0, o1);
+          store_n<T, VEC>(dst + half + i0, o2);
         }
       }
     }
-    store_n<T, VEC>(dst + i0, o1);
-    store_n<T, VEC>(dst + half + i0, o2);
   }
 }
 
@@ -112,6 +119,22 @@ __global__ void positions_kernel(const int32_t* __restrict__ cu, int ndoc, int32
   }
 }
 
+template <typename T, int VEC, bool BWD>
+void rope_launch(int hpt, unsigned grid, int block, int HP, cudaStream_t s, const void* q,
+                 const void* k, void* qo, void* ko, const int32_t* pos, const float* cs,
+                 int64_t max_pos, int64_t rows, int Hq, int Hk, int D) {
+#define GBLN_ROPE(N)                                                                      \
+  rope_kernel<T, VEC, BWD, N><<<grid, block, 0, s>>>((const T*)q, (const T*)k, (T*)qo,     \
+                                                     (T*)ko, pos, (const float2*)cs,       \
+                                                     max_pos, rows, Hq, Hk, D, HP)
+  switch (hpt) {
+    case 1: GBLN_ROPE(1); break;
+    case 2: GBLN_ROPE(2); break;
+    default: GBLN_ROPE(4); break;
+  }
+#undef GBLN_ROPE
+}
+
 template <typename T, bool BWD>
 gbln_status rope_typed(const void* q, const void* k, void* qo, void* ko, const int32_t* pos,
                        const float* cs, int64_t max_pos, int64_t rows, int Hq, int Hk, int D,
@@ -122,16 +145,22 @@ gbln_status rope_typed(const void* q, const void* k, void* qo, void* ko, const i
                    (Hk == 0 || (aligned16(k) && aligned16(ko)));
   const int sms = sm_count();
   if (sms <= 0) return GBLN_ERR_CUDA;
-  const int64_t cap = (int64_t)sms * (2048 / kRopeBlock) * 8;
-  if (vec) {
-    const int64_t units = rows * (int64_t)(Hq + Hk) * (half / VEC);
-    rope_kernel<T, VEC, BWD><<<grid_for(units, kRopeBlock, cap), kRopeBlock, 0, s>>>(
-        (const T*)q, (const T*)k, (T*)qo, (T*)ko, pos, (const float2*)cs, max_pos, rows, Hq, Hk, D);
-  } else {
-    const int64_t units = rows * (int64_t)(Hq + Hk) * half;
-    rope_kernel<T, 1, BWD><<<grid_for(units, kRopeBlock, cap), kRopeBlock, 0, s>>>(
-        (const T*)q, (const T*)k, (T*)qo, (T*)ko, pos, (const float2*)cs, max_pos, rows, Hq, Hk, D);
-  }
+  const int nvh = vec ? half / VEC : half;
+  if (nvh > 512) return GBLN_ERR_UNSUPPORTED;  // head size above 1024 (bf16 vector path: 8192)
+  const int HT = Hq + Hk;
+  // Heads per thread: the smallest of 1, 2, 4 that fits the block in 512 threads
+  // (4 with a loop over further heads beyond that).
+  int hpt = 1;
+  while (hpt < 4 && (int64_t)nvh * ((HT + hpt - 1) / hpt) > 512) hpt *= 2;
+  int HP = (HT + hpt - 1) / hpt;
+  if ((int64_t)nvh * HP > 512) HP = 512 / nvh;
+  const int block = nvh * HP;
+  const int per_sm = block > 0 ? 2048 / block : 1;
+  const unsigned grid = grid_for(rows, 1, (int64_t)sms * (per_sm > 0 ? per_sm : 1));
+  if (vec)
+    rope_launch<T, VEC, BWD>(hpt, grid, block, HP, s, q, k, qo, ko, pos, cs, max_pos, rows, Hq, Hk, D);
+  else
+    rope_launch<T, 1, BWD>(hpt, grid, block, HP, s, q, k, qo, ko, pos, cs, max_pos, rows, Hq, Hk, D);
   return launch_status();
 }
 
@@ -143,11 +172,11 @@ gbln_status rope_entry(const void* q, const void* k, void* qo, void* ko, const i
   if (T < 0 || Hq < 0 || Hk < 0 || Hq + Hk <= 0 || D <= 0 || (D & 1) || max_pos < 0)
     return GBLN_ERR_INVALID_ARG;
   if ((int64_t)(Hq + Hk) * D > (1 << 24)) return GBLN_ERR_INVALID_ARG;
+  if (T == 0) return GBLN_OK;  // nothing is read or written: pointers are not examined
   if (!pos || !cs) return GBLN_ERR_INVALID_ARG;
   if (Hq > 0 && (!q || !qo)) return GBLN_ERR_INVALID_ARG;
   if (Hk > 0 && (!k || !ko)) return GBLN_ERR_INVALID_ARG;
   if (((uintptr_t)cs & 7u) != 0) return GBLN_ERR_INVALID_ARG;  // float2 table
-  if (T == 0) return GBLN_OK;
   cudaStream_t s = (cudaStream_t)stream;
   if (io == GBLN_F32) return rope_typed<float, BWD>(q, k, qo, ko, pos, cs, max_pos, T, Hq, Hk, D, s);
   return rope_typed<bf16, BWD>(q, k, qo, ko, pos, cs, max_pos, T, Hq, Hk, D, s);

@@ -72,6 +72,7 @@ def test_rmsnorm_fwd_rejects(lib):
     assert _fwd(lib, io=F32, wt=BF16) == UNSUPPORTED
     assert _fwd(lib, T=0) == OK  # nothing to do, nothing launched
     assert _fwd(lib, T=0, r=FAKE, ho=FAKE, io=BF16, wt=F32) == OK
+    assert _fwd(lib, T=0, x=None, w=None, y=None, rstd=None) == OK  # empty tensors: null data
 
 
 def test_rmsnorm_bwd_and_finalize_reject(lib):
@@ -82,6 +83,7 @@ def test_rmsnorm_bwd_and_finalize_reject(lib):
         assert bwd(**kw) == INVALID, kw
     assert bwd(io=F32, wt=BF16) == UNSUPPORTED
     assert bwd(T=0) == OK
+    assert bwd(T=0, dy=None, h=None, part=None) == OK
     assert lib.gbln_rmsnorm_bwd_num_partials(-1, 8, BF16) == -1
     assert lib.gbln_rmsnorm_bwd_num_partials(4, 0, BF16) == -1
     assert lib.gbln_rmsnorm_bwd_num_partials(4, 8, 9) == -1
@@ -129,6 +131,7 @@ def test_swiglu_rejects(lib):
     assert lib.gbln_swiglu_fwd(FAKE, FAKE, FAKE, 1 << 40, 1 << 30, BF16, None) == INVALID
     assert lib.gbln_swiglu_fwd(FAKE, FAKE, FAKE, 4, 8, 2, None) == INVALID
     assert lib.gbln_swiglu_fwd(FAKE, FAKE, FAKE, 0, 8, BF16, None) == OK
+    assert lib.gbln_swiglu_fwd(None, None, None, 0, 8, BF16, None) == OK
     for i in range(5):
         args = [FAKE] * 5
         args[i] = None

@@ -10,7 +10,7 @@ import torch
 import oracle
 import rmsnorm_fwd_bwd_03_gb300 as gb
 
-from _checks import Guarded, check_dw, check_io, check_rstd, to64
+from _checks import Guarded, check_dw, check_io, check_rstd, dx_scale, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -61,8 +61,9 @@ def test_rmsnorm_shapes(T, H, io, wt, residual, offset):
         assert np.array_equal(to64(h), h_ref)
     check_io(to64(y), y_ref, io, "y")
     check_rstd(to64(rstd), rstd_ref)
-    dx_ref, dw_ref = oracle.rmsnorm_bwd(to64(dy), None if dres is None else to64(dres), h_ref, w64, eps)
-    check_io(to64(dx), dx_ref, io, "dx")
+    dres64 = None if dres is None else to64(dres)
+    dx_ref, dw_ref = oracle.rmsnorm_bwd(to64(dy), dres64, h_ref, w64, eps)
+    check_io(to64(dx), dx_ref, io, "dx", scale=dx_scale(to64(dy), w64, rstd_ref, dres64))
     check_dw(to64(dw), dw_ref)
 
 

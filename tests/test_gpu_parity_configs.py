@@ -20,7 +20,7 @@ import oracle
 import rmsnorm_fwd_bwd_03_gb300 as gb
 from rmsnorm_fwd_bwd_03_gb300.workload import ORDER, WORKLOADS, make_inputs
 
-from _checks import check_dw, check_io, check_rstd, sample_rows, to64
+from _checks import check_dw, check_io, check_rstd, dx_scale, sample_rows, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -71,7 +71,8 @@ def test_rmsnorm_fwd_bwd(name):
     check_io(to64(y.index_select(0, rows)), y_ref, wl.io, f"{name} y")
     check_rstd(to64(rstd.index_select(0, rows)), rstd_ref, f"{name} rstd")
     dx_ref, _ = oracle.rmsnorm_bwd(dy_s, dres_s, h_ref, w64, wl.eps)
-    check_io(to64(dx.index_select(0, rows)), dx_ref, wl.io, f"{name} dx")
+    check_io(to64(dx.index_select(0, rows)), dx_ref, wl.io, f"{name} dx",
+             scale=dx_scale(dy_s, w64, rstd_ref, dres_s))
 
 
 @pytest.mark.parametrize("name", ORDER)
