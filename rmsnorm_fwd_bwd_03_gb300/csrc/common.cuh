@@ -92,6 +92,30 @@ __device__ __forceinline__ void store_n(T* p, const float (&v)[N]) {
     for (int e = 0; e < N; ++e) p[e] = from_f32<T>(v[e]);
   }
 }
+// N elements of T kept in their storage format between load and use (one
+// 16-byte register quad on the vector path, N scalars otherwise), so that many
+// loads can be in flight without holding their float32 expansion.
+template <typename T, int N, bool VECTOR = (N * sizeof(T) == 16)>
+struct Packed;
+template <typename T, int N>
+struct Packed<T, N, true> {
+  uint4 r;
+  __device__ __forceinline__ void load(const T* p) { r = ld_stream(p); }
+  __device__ __forceinline__ void get(float (&v)[N]) const { unpack<N>(r, v); }
+};
+template <typename T, int N>
+struct Packed<T, N, false> {
+  T r[N];
+  __device__ __forceinline__ void load(const T* p) {
+#pragma unroll
+    for (int e = 0; e < N; ++e) r[e] = p[e];
+  }
+  __device__ __forceinline__ void get(float (&v)[N]) const {
+#pragma unroll
+    for (int e = 0; e < N; ++e) v[e] = to_f32(r[e]);
+  }
+};
+
 // Round float32 values to T and back (what a store followed by a load would see).
 template <typename T, int N>
 __device__ __forceinline__ void round_to(float (&v)[N]) {

@@ -294,24 +294,29 @@ rms_bwd_generic(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
 }
 
 // ---------------------------------------------------------------------------
-// Finalize: dw[j] = (acc ? dw[j] : 0) + sum_p partial[p, j].  Block (32, 8):
-// column j = 32 * blockIdx.x + tx; row stripe ty sums p = ty, ty + 8, ... in
-// order, then the 8 stripes are added in order.
+// Finalize: dw[j] = (acc ? dw[j] : 0) + sum_p partial[p, j].  Block (32, 16):
+// column j = 32 * blockIdx.x + tx; row stripe ty sums p = ty, ty + 16, ... in
+// order (loads unrolled so several are in flight; the additions stay in that
+// order), then the 16 stripes are added in order.  Bitwise reproducible.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
+constexpr int kFinStripes = 16;
+
+__global__ void __launch_bounds__(32 * kFinStripes)
 rms_dw_finalize(const float* __restrict__ partial, int64_t P, int H, float* dw, int accumulate) {
-  __shared__ float s[8][33];
+  __shared__ float s[kFinStripes][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int j = blockIdx.x * 32 + tx;
   float a = 0.f;
-  if (j < H)
-    for (int64_t q = ty; q < P; q += 8) a += partial[(size_t)q * H + j];
+  if (j < H) {
+#pragma unroll 8
+    for (int64_t q = ty; q < P; q += kFinStripes) a += __ldg(partial + (size_t)q * H + j);
+  }
   s[ty][tx] = a;
   __syncthreads();
   if (ty == 0 && j < H) {
     float t = 0.f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) t += s[q][tx];
+    for (int q = 0; q < kFinStripes; ++q) t += s[q][tx];
     dw[j] = accumulate ? dw[j] + t : t;
   }
 }
@@ -524,6 +529,6 @@ extern "C" gbln_status gbln_rmsnorm_dw_finalize(const float* dw_partial, int64_t
   if (!dw || (P > 0 && !dw_partial)) return GBLN_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   const unsigned grid = (unsigned)((H + 31) / 32);
-  rms_dw_finalize<<<grid, 256, 0, s>>>(dw_partial, P, (int)H, dw, accumulate ? 1 : 0);
+  rms_dw_finalize<<<grid, 32 * kFinStripes, 0, s>>>(dw_partial, P, (int)H, dw, accumulate ? 1 : 0);
   return launch_status();
 }

@@ -9,10 +9,10 @@
 //
 // HBM-bound design: one thread moves the two 16-byte vectors at i and i + D/2
 // of a head row, so each element is read and written exactly once (in place is
-// allowed).  A block covers all heads of one token at a time; each thread
-// reads the token's position and its slice of the cos/sin row (float32, from a
-// table built once in double precision, served from L1 / L2) once and applies
-// it to every head it owns.  No integer division in the token loop.
+// allowed).  A block covers all heads of a few consecutive tokens at a time;
+// each thread reads a token's position and its slice of the cos/sin row
+// (float32, from a table built once in double precision, served from L1 / L2)
+// once and applies it to every head it owns.  No integer division in the loop.
 
 #include "common.cuh"
 
@@ -20,12 +20,85 @@ namespace gbln {
 
 namespace {
 
+// Rotate one vector pair: elements i0.. of the first half (a) and of the second
+// half (b) of a head row, with the cos/sin entries c[0..VEC).  On the vector
+// path the work goes two elements (one 32-bit word of bf16, or two floats) at
+// a time so that only the packed inputs and one float4 of cos/sin are live.
+template <typename T, int VEC, bool BWD>
+__device__ __forceinline__ void rotate_store(const Packed<T, VEC>& a, const Packed<T, VEC>& b,
+                                             const float2* c, bool ok, T* d1, T* d2) {
+  const float qnan = __int_as_float(0x7fc00000);
+  if constexpr (VEC * sizeof(T) == 16) {
+    const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a.r);
+    const uint32_t* bw = reinterpret_cast<const uint32_t*>(&b.r);
+    uint32_t o1[4], o2[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float x1[2], x2[2];
+      if constexpr (sizeof(T) == 2) {
+        x1[0] = bf16_lo(aw[w]); x1[1] = bf16_hi(aw[w]);
+        x2[0] = bf16_lo(bw[w]); x2[1] = bf16_hi(bw[w]);
+      } else {
+        x1[0] = __uint_as_float(aw[w]); x2[0] = __uint_as_float(bw[w]);
+      }
+      constexpr int PER = sizeof(T) == 2 ? 2 : 1;  // elements per 32-bit word
+      float cv[2], sv[2];
+      if constexpr (PER == 2) {
+        const float4 f = ok ? __ldg(reinterpret_cast<const float4*>(c + 2 * w))
+                            : make_float4(qnan, qnan, qnan, qnan);
+        cv[0] = f.x; sv[0] = f.y; cv[1] = f.z; sv[1] = f.w;
+      } else {
+        const float2 f = ok ? __ldg(c + w) : make_float2(qnan, qnan);
+        cv[0] = f.x; sv[0] = f.y;
+      }
+      float y1[2], y2[2];
+#pragma unroll
+      for (int e = 0; e < PER; ++e) {
+        if constexpr (!BWD) {
+          y1[e] = x1[e] * cv[e] - x2[e] * sv[e];
+          y2[e] = x2[e] * cv[e] + x1[e] * sv[e];
+        } else {
+          y1[e] = x1[e] * cv[e] + x2[e] * sv[e];
+          y2[e] = x2[e] * cv[e] - x1[e] * sv[e];
+        }
+      }
+      if constexpr (PER == 2) {
+        o1[w] = pack_bf16x2(y1[0], y1[1]);
+        o2[w] = pack_bf16x2(y2[0], y2[1]);
+      } else {
+        o1[w] = __float_as_uint(y1[0]);
+        o2[w] = __float_as_uint(y2[0]);
+      }
+    }
+    st_vec(d1, make_uint4(o1[0], o1[1], o1[2], o1[3]));
+    st_vec(d2, make_uint4(o2[0], o2[1], o2[2], o2[3]));
+  } else {
+    float x1[VEC], x2[VEC], y1[VEC], y2[VEC];
+    a.get(x1);
+    b.get(x2);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      const float2 f = ok ? __ldg(c + e) : make_float2(qnan, qnan);
+      if constexpr (!BWD) {
+        y1[e] = x1[e] * f.x - x2[e] * f.y;
+        y2[e] = x2[e] * f.x + x1[e] * f.y;
+      } else {
+        y1[e] = x1[e] * f.x + x2[e] * f.y;
+        y2[e] = x2[e] * f.x - x1[e] * f.y;
+      }
+    }
+    store_n<T, VEC>(d1, y1);
+    store_n<T, VEC>(d2, y2);
+  }
+}
+
 // Block of HP * NVH threads, NVH = D/2/VEC vectors per half head row: thread
 // (hl, v) owns vector v (elements v*VEC.. and D/2 + v*VEC..) of heads hl,
-// hl + HP, ... of every token the block visits; tokens are strided by gridDim.
-// The cos/sin vector of a token is loaded once per thread and reused for all
-// its heads; up to HPT heads' loads are issued before any of them is used.
-template <typename T, int VEC, bool BWD, int HPT>
+// hl + HP, ... (HPT of them per pass) of UT consecutive tokens per iteration;
+// token groups are strided by gridDim.  All UT * HPT head loads are issued
+// before the first is used, and they do not wait on the position -> cos/sin
+// lookup, which is served from L1 / L2 and reused across the thread's heads.
+template <typename T, int VEC, bool BWD, int HPT, int UT>
 __global__ void __launch_bounds__(512)
 rope_kernel(const T* q, const T* k, T* qo, T* ko, const int32_t* __restrict__ pos,
             const float2* __restrict__ cs, int64_t max_pos, int64_t T_, int Hq, int Hk,
@@ -36,55 +109,39 @@ rope_kernel(const T* q, const T* k, T* qo, T* ko, const int32_t* __restrict__ po
   const int hl = threadIdx.x / nvh;
   const int HT = Hq + Hk;
   const int i0 = v * VEC;
-  for (int64_t t = blockIdx.x; t < T_; t += gridDim.x) {
-    const int p = __ldg(pos + t);
-    const bool ok = p >= 0 && (int64_t)p < max_pos;
-    float cv[VEC], sv[VEC];
-    if (ok) {
-      const float2* c = cs + (size_t)p * half + i0;
-      if constexpr (VEC % 2 == 0) {
+  for (int64_t tb = (int64_t)blockIdx.x * UT; tb < T_; tb += (int64_t)gridDim.x * UT) {
+    int p[UT];
 #pragma unroll
-        for (int e = 0; e < VEC; e += 2) {
-          const float4 f = __ldg(reinterpret_cast<const float4*>(c + e));
-          cv[e] = f.x; sv[e] = f.y; cv[e + 1] = f.z; sv[e + 1] = f.w;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) { const float2 f = __ldg(c + e); cv[e] = f.x; sv[e] = f.y; }
-      }
-    } else {  // out-of-range position: never read the table, emit NaN
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) { cv[e] = __int_as_float(0x7fc00000); sv[e] = cv[e]; }
-    }
+    for (int u = 0; u < UT; ++u) p[u] = tb + u < T_ ? __ldg(pos + tb + u) : 0;
     for (int h0 = hl; h0 < HT; h0 += HP * HPT) {
-      float a[HPT][VEC], b[HPT][VEC];
+      Packed<T, VEC> a[UT][HPT], b[UT][HPT];
 #pragma unroll
-      for (int j = 0; j < HPT; ++j) {
-        const int h = h0 + j * HP;
-        if (h < HT) {
-          const T* src = h < Hq ? q + ((size_t)t * Hq + h) * D : k + ((size_t)t * Hk + (h - Hq)) * D;
-          load_n<T, VEC>(src + i0, a[j]);
-          load_n<T, VEC>(src + half + i0, b[j]);
+      for (int u = 0; u < UT; ++u) {
+        const int64_t t = tb + u;
+#pragma unroll
+        for (int j = 0; j < HPT; ++j) {
+          const int h = h0 + j * HP;
+          if (t < T_ && h < HT) {
+            const T* src = h < Hq ? q + ((size_t)t * Hq + h) * D : k + ((size_t)t * Hk + (h - Hq)) * D;
+            a[u][j].load(src + i0);
+            b[u][j].load(src + half + i0);
+          }
         }
       }
 #pragma unroll
-      for (int j = 0; j < HPT; ++j) {
-        const int h = h0 + j * HP;
-        if (h < HT) {
-          T* dst = h < Hq ? qo + ((size_t)t * Hq + h) * D : ko + ((size_t)t * Hk + (h - Hq)) * D;
-          float o1[VEC], o2[VEC];
+      for (int u = 0; u < UT; ++u) {
+        const int64_t t = tb + u;
+        if (t >= T_) break;
+        // out-of-range position: the table is not read and the outputs are NaN
+        const bool ok = p[u] >= 0 && (int64_t)p[u] < max_pos;
+        const float2* c = cs + (ok ? (size_t)p[u] * half : 0) + i0;
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            if constexpr (!BWD) {
-              o1[e] = a[j][e] * cv[e] - b[j][e] * sv[e];
-              o2[e] = b[j][e] * cv[e] + a[j][e] * sv[e];
-            } else {
-              o1[e] = a[j][e] * cv[e] + b[j][e] * sv[e];
-              o2[e] = b[j][e] * cv[e] - a[j][e] * sv[e];
-            }
+        for (int j = 0; j < HPT; ++j) {
+          const int h = h0 + j * HP;
+          if (h < HT) {
+            T* dst = h < Hq ? qo + ((size_t)t * Hq + h) * D : ko + ((size_t)t * Hk + (h - Hq)) * D;
+            rotate_store<T, VEC, BWD>(a[u][j], b[u][j], c, ok, dst + i0, dst + half + i0);
           }
-          store_n<T, VEC>(dst + i0, o1);
-          store_n<T, VEC>(dst + half + i0, o2);
         }
       }
     }
@@ -123,14 +180,14 @@ template <typename T, int VEC, bool BWD>
 void rope_launch(int hpt, unsigned grid, int block, int HP, cudaStream_t s, const void* q,
                  const void* k, void* qo, void* ko, const int32_t* pos, const float* cs,
                  int64_t max_pos, int64_t rows, int Hq, int Hk, int D) {
-#define GBLN_ROPE(N)                                                                      \
-  rope_kernel<T, VEC, BWD, N><<<grid, block, 0, s>>>((const T*)q, (const T*)k, (T*)qo,     \
-                                                     (T*)ko, pos, (const float2*)cs,       \
-                                                     max_pos, rows, Hq, Hk, D, HP)
-  switch (hpt) {
-    case 1: GBLN_ROPE(1); break;
-    case 2: GBLN_ROPE(2); break;
-    default: GBLN_ROPE(4); break;
+#define GBLN_ROPE(N, U)                                                                   \
+  rope_kernel<T, VEC, BWD, N, U><<<grid, block, 0, s>>>((const T*)q, (const T*)k, (T*)qo,  \
+                                                        (T*)ko, pos, (const float2*)cs,    \
+                                                        max_pos, rows, Hq, Hk, D, HP)
+  switch (hpt) {  // heads x tokens per thread and pass
+    case 1: GBLN_ROPE(1, 2); break;
+    case 2: GBLN_ROPE(2, 1); break;
+    default: GBLN_ROPE(4, 1); break;
   }
 #undef GBLN_ROPE
 }
@@ -156,7 +213,8 @@ gbln_status rope_typed(const void* q, const void* k, void* qo, void* ko, const i
   if ((int64_t)nvh * HP > 512) HP = 512 / nvh;
   const int block = nvh * HP;
   const int per_sm = block > 0 ? 2048 / block : 1;
-  const unsigned grid = grid_for(rows, 1, (int64_t)sms * (per_sm > 0 ? per_sm : 1));
+  const int ut = hpt == 1 ? 2 : 1;
+  const unsigned grid = grid_for((rows + ut - 1) / ut, 1, (int64_t)sms * (per_sm > 0 ? per_sm : 1));
   if (vec)
     rope_launch<T, VEC, BWD>(hpt, grid, block, HP, s, q, k, qo, ko, pos, cs, max_pos, rows, Hq, Hk, D);
   else
