@@ -263,6 +263,41 @@ def time_oracle(wl, rows, budget_s):
 
 # ---------------------------------------------------------------------------
 
+def run_single_op(args, wl, device):
+    """Time one operator of the step alone: W untimed launches, then K launches,
+    each timed with CUDA events, L2 flushed in between.  One JSON line."""
+    from rmsnorm_fwd_bwd_03_gb300.workload import scaled
+    from rmsnorm_fwd_bwd_03_gb300._build import build_library
+    build_library()
+    if args.tokens:
+        wl = scaled(wl, args.tokens, f"_T{args.tokens}")
+    step = Step(wl, device, seed=0)
+    stream = torch.cuda.current_stream(device)
+    calls = step.calls(stream.cuda_stream)
+    run_calls(calls)  # every output of the step exists (h, rstd, positions, partials)
+    call = [c for c in calls if c[0] == args.op]
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+    for _ in range(args.warmup):
+        flush.zero_()
+        run_calls(call)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(call) + 1)]
+        run_calls(call, ev)
+        times.append(ev)
+    torch.cuda.synchronize()
+    ms = sum(e[0].elapsed_time(e[-1]) for e in times) / args.steps
+    alg = wl.algorithmic_bytes()[args.op]
+    peak, peak_kind = _measured_peak()
+    gbs = alg / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
+    print(json.dumps({"op": args.op, "workload": wl.name, "tokens": wl.T, "launches": args.steps,
+                      "ms_per_launch": ms, "alg_bytes": alg, "GB/s": round(gbs, 1),
+                      "frac": round(gbs / peak, 4), "peak": peak, "peak_kind": f"of {peak_kind}"}))
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -295,6 +330,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--op", choices=OPS, default=None,
+                    help="time one operator alone (also the driver for ncu captures)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="with --op: use the workload's widths with this many tokens")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -341,6 +380,9 @@ def main():
     device = torch.device("cuda", local)
     from rmsnorm_fwd_bwd_03_gb300._build import build_library
     build_library()
+
+    if args.op:
+        return run_single_op(args, wl, device)
 
     step = Step(wl, device, seed=rank)
     stream = torch.cuda.current_stream(device)
