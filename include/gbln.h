@@ -137,6 +137,37 @@ gbln_status gbln_rmsnorm_bwd(const void* dy, const void* dresidual_out, const vo
 gbln_status gbln_rmsnorm_dw_finalize(const float* dw_partial, int64_t P, int64_t H,
                                      float* dw, int accumulate, gbln_stream_t stream);
 
+/*
+ * Backward without a caller-provided workspace: dx as gbln_rmsnorm_bwd, and the
+ * finished weight gradient dw [H] float32 (as gbln_rmsnorm_dw_finalize with
+ * accumulate = 0), in two launches on `stream`.  The sources have no
+ * counterpart of this entry point; it exists for callers that cannot allocate
+ * device memory where they run the backward pass (a region being recorded into
+ * a CUDA graph under a capture mode that forbids cudaMalloc, a runtime whose
+ * device memory belongs to a pool it may not bypass, a latency-critical loop in
+ * which an allocation could synchronise the device).  The caller still passes
+ * every input and output.
+ *
+ * Scratch: the dW partial rows live in one fixed array inside the library
+ * (4 Mi float32 = 16 MiB, held by every GPU that loads the library until the
+ * process exits).  Every call on a device uses the same array and overwrites the
+ * rows it reads, so nothing needs clearing; calls that may overlap on the GPU
+ * (other streams, other threads) race on it and must be serialised by the caller.
+ * The usual number of partial rows is reduced when it would not fit, so the
+ * summation order (still fixed for a shape and GPU) can differ from
+ * gbln_rmsnorm_bwd's by float32 rounding.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.
+ * Errors: as gbln_rmsnorm_bwd; GBLN_ERR_WORKSPACE if H > 4 Mi (a partial row
+ * would not fit); GBLN_ERR_CUDA if the address lookup fails.  T == 0 sets dw to
+ * zero (one launch).  dx may alias dy or dresidual_out exactly.
+ */
+gbln_status gbln_rmsnorm_bwd_noalloc(const void* dy, const void* dresidual_out, const void* h,
+                                     const void* weight, const float* rstd,
+                                     void* dx, float* dw, int64_t T, int64_t H,
+                                     gbln_dtype io, gbln_dtype wt, gbln_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* Rotary position embedding on Q and K ([FL] attention with RoPE, rotary     */
 /* type default with theta; [LF] fused RoPE; [HF] §Liger)                     */

@@ -20,6 +20,7 @@ from ._build import LIB as _LIB_PATH
 __all__ = [
     "GblnError", "library", "library_path", "status_string", "version",
     "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_num_partials", "rmsnorm_dw_finalize",
+    "rmsnorm_bwd_noalloc",
     "rope_table", "rope_fwd", "rope_bwd", "positions_from_cu_seqlens",
     "swiglu_fwd", "swiglu_bwd",
     "F32", "BF16",
@@ -43,6 +44,7 @@ _SIGNATURES = {
     "gbln_rmsnorm_bwd_num_partials": (_i64, [_i64, _i64, ctypes.c_int]),
     "gbln_rmsnorm_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
     "gbln_rmsnorm_dw_finalize": (ctypes.c_int, [_vp, _i64, _i64, _vp, ctypes.c_int, _vp]),
+    "gbln_rmsnorm_bwd_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
     "gbln_rope_table": (ctypes.c_int, [_vp, _i64, _i32, _f64, _vp]),
     "gbln_rope_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, ctypes.c_int, _vp]),
     "gbln_rope_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, ctypes.c_int, _vp]),
@@ -183,6 +185,23 @@ def rmsnorm_dw_finalize(dw_partial, P, dw=None, accumulate=False):
         _stream(dw_partial))
     _check("gbln_rmsnorm_dw_finalize", st)
     return dw
+
+
+def rmsnorm_bwd_noalloc(dy, h, weight, rstd, dresidual_out=None, *, dx=None, dw=None):
+    """``gbln_rmsnorm_bwd_noalloc``: dx and the finished float32 dW [H] with no workspace
+    argument; the library's fixed internal scratch holds the partial sums, so calls
+    that may overlap on the GPU must be serialised.  Returns ``(dx, dw)``."""
+    H = dy.shape[-1]
+    T = dy.numel() // H if H else 0
+    if dx is None:
+        dx = torch.empty_like(dy)
+    if dw is None:
+        dw = torch.empty(H, dtype=torch.float32, device=dy.device)
+    st = library().gbln_rmsnorm_bwd_noalloc(
+        _opt(dy, "dy"), _opt(dresidual_out, "dresidual_out"), _opt(h, "h"), _dev(weight, "weight"),
+        _opt(rstd, "rstd"), _opt(dx, "dx"), _dev(dw, "dw"), T, H, _io(dy), _io(weight), _stream(dw))
+    _check("gbln_rmsnorm_bwd_noalloc", st)
+    return dx, dw
 
 
 # ---------------------------------------------------------------------------

@@ -13,6 +13,8 @@
 // launch sums the partial rows in a fixed order.  No atomics: bitwise
 // reproducible for a fixed shape and SM count.
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace gbln {
@@ -530,5 +532,84 @@ extern "C" gbln_status gbln_rmsnorm_dw_finalize(const float* dw_partial, int64_t
   cudaStream_t s = (cudaStream_t)stream;
   const unsigned grid = (unsigned)((H + 31) / 32);
   rms_dw_finalize<<<grid, 32 * kFinStripes, 0, s>>>(dw_partial, P, (int)H, dw, accumulate ? 1 : 0);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// Backward without caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// backward pass: code recorded into a CUDA graph under a capture mode that
+// forbids cudaMalloc, runtimes whose memory is owned by a pool they may not
+// bypass, and latency-critical loops where an allocation could synchronise
+// the device.  For them the dW partials live in the fixed array below, which
+// is part of the loaded module: every GPU that loads the library holds it
+// (16 MiB) until the process exits.
+// ---------------------------------------------------------------------------
+namespace gbln {
+namespace {
+
+constexpr int64_t kScratchFloats = 4LL << 20;  // 16 MiB of float32 dW partials
+static __device__ __align__(256) float g_dw_scratch[kScratchFloats];
+
+constexpr int kMaxScratchDevices = 64;
+std::atomic<float*> g_scratch_ptr[kMaxScratchDevices];
+
+// Device address of g_dw_scratch on the current device (looked up once per
+// device; in host code the symbol itself is only a host-side stand-in).
+float* scratch_on_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  float* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_dw_scratch) != cudaSuccess || addr == nullptr) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  p = static_cast<float*>(addr);
+  g_scratch_ptr[dev].store(p, std::memory_order_release);
+  return p;
+}
+
+}  // namespace
+}  // namespace gbln
+
+extern "C" gbln_status gbln_rmsnorm_bwd_noalloc(const void* dy, const void* dresidual_out,
+                                                const void* h, const void* weight,
+                                                const float* rstd, void* dx, float* dw,
+                                                int64_t T, int64_t H, gbln_dtype io,
+                                                gbln_dtype wt, gbln_stream_t stream) {
+  if (!dtype_ok(io) || !dtype_ok(wt)) return GBLN_ERR_INVALID_ARG;
+  if (T < 0 || T > kMaxRows || H <= 0 || H > kMaxH) return GBLN_ERR_INVALID_ARG;
+  if (!dtypes_ok(io, wt)) return GBLN_ERR_UNSUPPORTED;
+  if (H > kScratchFloats) return GBLN_ERR_WORKSPACE;  // one partial row must fit
+  if (!dw) return GBLN_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (T == 0) {  // no rows: dW = 0
+    rms_dw_finalize<<<(unsigned)((H + 31) / 32), 32 * kFinStripes, 0, s>>>(nullptr, 0, (int)H, dw, 0);
+    return launch_status();
+  }
+  if (!dy || !h || !weight || !rstd || !dx) return GBLN_ERR_INVALID_ARG;
+  const int sms = sm_count();
+  if (sms <= 0) return GBLN_ERR_CUDA;
+  float* scratch = scratch_on_current_device();
+  if (!scratch) return GBLN_ERR_CUDA;
+  // Same kernels as gbln_rmsnorm_bwd + gbln_rmsnorm_dw_finalize; fewer partial
+  // rows when the usual count would not fit the fixed array.
+  int64_t P = partials_for(T, geometry(H, dtype_size(io)), sms);
+  if (P * H > kScratchFloats) P = kScratchFloats / H;
+  gbln_status st;
+  if (io == GBLN_F32)
+    st = bwd_typed<float, float>(dy, dresidual_out, h, weight, rstd, dx, scratch, P, T, H, s);
+  else if (wt == GBLN_BF16)
+    st = bwd_typed<bf16, bf16>(dy, dresidual_out, h, weight, rstd, dx, scratch, P, T, H, s);
+  else
+    st = bwd_typed<bf16, float>(dy, dresidual_out, h, weight, rstd, dx, scratch, P, T, H, s);
+  if (st != GBLN_OK) return st;
+  rms_dw_finalize<<<(unsigned)((H + 31) / 32), 32 * kFinStripes, 0, s>>>(scratch, P, (int)H, dw, 0);
   return launch_status();
 }
