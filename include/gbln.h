@@ -69,6 +69,16 @@ const char* gbln_status_string(int status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int gbln_version(void);
 
+/*
+ * Per-device error word of the current device.  Kernels that wait on their own
+ * asynchronous (TMA bulk) copies bound every wait; if a bound is ever exceeded
+ * the kernel ORs bit 1 (wait timeout) into this word and stops early instead of
+ * hanging, so its outputs are then incomplete.  *code receives the word; clear
+ * != 0 resets it to zero.  Synchronous (device-wide copy): call it outside hot
+ * loops.  Errors: INVALID_ARG for a null code, CUDA if the device is unreachable.
+ */
+gbln_status gbln_device_error(uint32_t* code, int clear);
+
 /* ------------------------------------------------------------------------- */
 /* RMSNorm with fused residual add ([FL] Transformer Block 结构, 训练配置示例;  */
 /* [LF] fused RMSNorm; [HF] §Liger)                                          */

@@ -18,7 +18,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 
 __all__ = [
-    "GblnError", "library", "library_path", "status_string", "version",
+    "GblnError", "library", "library_path", "status_string", "version", "device_error",
     "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_num_partials", "rmsnorm_dw_finalize",
     "rmsnorm_bwd_noalloc",
     "rope_table", "rope_fwd", "rope_bwd", "positions_from_cu_seqlens",
@@ -40,6 +40,7 @@ _f64 = ctypes.c_double
 _SIGNATURES = {
     "gbln_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gbln_version": (ctypes.c_int, []),
+    "gbln_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "gbln_rmsnorm_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, ctypes.c_int, ctypes.c_int, _vp]),
     "gbln_rmsnorm_bwd_num_partials": (_i64, [_i64, _i64, ctypes.c_int]),
     "gbln_rmsnorm_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
@@ -92,6 +93,13 @@ def status_string(status: int) -> str:
 
 def version() -> int:
     return library().gbln_version()
+
+
+def device_error(clear: bool = False) -> int:
+    """``gbln_device_error``: the current device's error word (0 = no kernel gave up a wait)."""
+    v = ctypes.c_uint32(0)
+    _check("gbln_device_error", library().gbln_device_error(ctypes.byref(v), 1 if clear else 0))
+    return int(v.value)
 
 
 def _check(fn, status):

@@ -10,7 +10,29 @@ namespace gbln {
 namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];  // 0 = not yet queried
+std::atomic<unsigned int*> g_err_ptr[kMaxDevices];
+// Per-device error word: kernels that wait on asynchronous copies OR in a bit
+// here when a wait exceeds its bound (they then stop instead of hanging).
+__device__ unsigned int g_device_error;
 }  // namespace
+
+unsigned int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  unsigned int* p = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess || !addr) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  p = static_cast<unsigned int*>(addr);
+  g_err_ptr[dev].store(p, std::memory_order_release);
+  return p;
+}
 
 int sm_count() {
   int dev = 0;
@@ -43,3 +65,23 @@ extern "C" const char* gbln_status_string(int status) {
 }
 
 extern "C" int gbln_version(void) { return 100; }
+
+extern "C" gbln_status gbln_device_error(uint32_t* code, int clear) {
+  if (!code) return GBLN_ERR_INVALID_ARG;
+  unsigned int* p = gbln::device_error_word();
+  if (!p) return GBLN_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return GBLN_ERR_CUDA;
+  }
+  *code = v;
+  if (clear && v) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      return GBLN_ERR_CUDA;
+    }
+  }
+  return GBLN_OK;
+}

@@ -14,6 +14,8 @@
 // (float32, from a table built once in double precision, served from L1 / L2)
 // once and applies it to every head it owns.  No integer division in the loop.
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace gbln {
@@ -24,7 +26,9 @@ namespace {
 // half (b) of a head row, with the cos/sin entries c[0..VEC).  On the vector
 // path the work goes two elements (one 32-bit word of bf16, or two floats) at
 // a time so that only the packed inputs and one float4 of cos/sin are live.
-template <typename T, int VEC, bool BWD>
+// TABLE_IN_SMEM: c points into shared memory (plain loads) instead of the
+// global table (read-only cached loads).
+template <typename T, int VEC, bool BWD, bool TABLE_IN_SMEM = false>
 __device__ __forceinline__ void rotate_store(const Packed<T, VEC>& a, const Packed<T, VEC>& b,
                                              const float2* c, bool ok, T* d1, T* d2) {
   const float qnan = __int_as_float(0x7fc00000);
@@ -44,11 +48,11 @@ __device__ __forceinline__ void rotate_store(const Packed<T, VEC>& a, const Pack
       constexpr int PER = sizeof(T) == 2 ? 2 : 1;  // elements per 32-bit word
       float cv[2], sv[2];
       if constexpr (PER == 2) {
-        const float4 f = ok ? __ldg(reinterpret_cast<const float4*>(c + 2 * w))
-                            : make_float4(qnan, qnan, qnan, qnan);
+        const float4* c4 = reinterpret_cast<const float4*>(c + 2 * w);
+        const float4 f = ok ? (TABLE_IN_SMEM ? *c4 : __ldg(c4)) : make_float4(qnan, qnan, qnan, qnan);
         cv[0] = f.x; sv[0] = f.y; cv[1] = f.z; sv[1] = f.w;
       } else {
-        const float2 f = ok ? __ldg(c + w) : make_float2(qnan, qnan);
+        const float2 f = ok ? (TABLE_IN_SMEM ? c[w] : __ldg(c + w)) : make_float2(qnan, qnan);
         cv[0] = f.x; sv[0] = f.y;
       }
       float y1[2], y2[2];
@@ -78,7 +82,7 @@ __device__ __forceinline__ void rotate_store(const Packed<T, VEC>& a, const Pack
     b.get(x2);
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-      const float2 f = ok ? __ldg(c + e) : make_float2(qnan, qnan);
+      const float2 f = ok ? (TABLE_IN_SMEM ? c[e] : __ldg(c + e)) : make_float2(qnan, qnan);
       if constexpr (!BWD) {
         y1[e] = x1[e] * f.x - x2[e] * f.y;
         y2[e] = x2[e] * f.x + x1[e] * f.y;
@@ -145,6 +149,148 @@ rope_kernel(const T* q, const T* k, T* qo, T* ko, const int32_t* __restrict__ po
         }
       }
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Staged path: a persistent block walks tiles of TT consecutive tokens.  One
+// producer thread reads the tile's positions and fills a stage of a ring of S
+// shared-memory stages with TMA bulk copies: the tile's Q rows and K rows (two
+// contiguous runs) and each token's cos/sin row from the table, all completing
+// on the stage's mbarrier.  S tiles stay in flight per block without holding
+// registers, and the threads then work from shared memory only: rotate and
+// store straight to global memory with 128-bit stores.  Thread (r, v): vector
+// v of the half rows, head lanes r, r + HPL, ...
+// Stage layout: [TT Q rows][TT K rows][TT cos/sin rows][TT positions].
+// ---------------------------------------------------------------------------
+constexpr int kRopeStages = 4;
+constexpr int kStagedMaxThreads = 32 + 256;  // producer warp + up to 8 consumer warps
+// Bytes of Q, K and cos/sin rows per stage (whole tokens; at least one token).
+constexpr size_t kStageTarget = 24 * 1024;
+
+struct StageGeom {
+  size_t qrow, krow, csrow, stage;
+  int TT;
+  __host__ __device__ size_t cs_off() const { return (size_t)TT * (qrow + krow); }
+  __host__ __device__ size_t pos_off() const { return cs_off() + (size_t)TT * csrow; }
+};
+
+template <typename T>
+__host__ __device__ inline StageGeom stage_geom(int Hq, int Hk, int D, int TT) {
+  StageGeom g;
+  g.qrow = (size_t)Hq * D * sizeof(T);
+  g.krow = (size_t)Hk * D * sizeof(T);
+  g.csrow = (size_t)(D / 2) * sizeof(float2);
+  g.TT = TT;
+  g.stage = g.pos_off() + (((size_t)TT * sizeof(int) + 15) / 16) * 16;
+  return g;
+}
+
+// Warp 0 is the producer (its lane 0 issues); warps 1.. consume.  full[s]
+// completes when stage s holds its tile; empty[s] completes when every
+// consumer warp has finished reading it.  All waits are bounded.
+template <typename T, bool BWD>
+__global__ void __launch_bounds__(kStagedMaxThreads)
+rope_staged_kernel(const T* __restrict__ q, const T* __restrict__ k, T* qo, T* ko,
+                   const int32_t* __restrict__ pos, const float2* __restrict__ cs,
+                   int64_t max_pos, int64_t T_, int Hq, int Hk, int D, int TT, int HPL,
+                   unsigned int* err) {
+  constexpr int VEC = VecOf<T>::N;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ uint64_t full[kRopeStages], empty[kRopeStages];
+  const int half = D / 2, nvh = half / VEC, HT = Hq + Hk;
+  const int ncw = (int)(blockDim.x / 32) - 1;  // consumer warps
+  const StageGeom g = stage_geom<T>(Hq, Hk, D, TT);
+  const int64_t ntiles = (T_ + TT - 1) / TT;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kRopeStages; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], ncw);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    if (lane != 0) return;
+    // ---- producer ----
+    int64_t j = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+      const int st = (int)(j % kRopeStages);
+      if (j >= kRopeStages &&
+          !mbar_wait(&empty[st], (uint32_t)(((j / kRopeStages) - 1) & 1), kWaitPolls)) {
+        atomicOr(err, kErrWaitTimeout);
+        break;
+      }
+      fence_proxy_async_smem();
+      const int64_t t0 = tile * TT;
+      const int ntok = (int)(T_ - t0 < TT ? T_ - t0 : (int64_t)TT);
+      unsigned char* base = smem + (size_t)st * g.stage;
+      int* spos = reinterpret_cast<int*>(base + g.pos_off());
+      uint32_t bytes = (uint32_t)(ntok * (g.qrow + g.krow));
+      for (int tok = 0; tok < ntok; ++tok) {
+        const int p = __ldg(pos + t0 + tok);
+        const bool ok = p >= 0 && (int64_t)p < max_pos;
+        spos[tok] = ok ? p : -1;
+        if (ok) bytes += (uint32_t)g.csrow;
+      }
+      mbar_arrive_expect_tx(&full[st], bytes);  // also releases the spos writes
+      bulk_load(base, reinterpret_cast<const unsigned char*>(q) + t0 * g.qrow,
+                (uint32_t)(ntok * g.qrow), &full[st]);
+      if (g.krow)
+        bulk_load(base + (size_t)TT * g.qrow, reinterpret_cast<const unsigned char*>(k) + t0 * g.krow,
+                  (uint32_t)(ntok * g.krow), &full[st]);
+      for (int tok = 0; tok < ntok; ++tok)
+        if (spos[tok] >= 0)
+          bulk_load(base + g.cs_off() + (size_t)tok * g.csrow, cs + (size_t)spos[tok] * half,
+                    (uint32_t)g.csrow, &full[st]);
+    }
+    // Do not leave while copies into this block's shared memory are in flight.
+    for (int64_t jj = (j > kRopeStages ? j - kRopeStages : 0); jj < j; ++jj)
+      mbar_wait(&full[jj % kRopeStages], (uint32_t)((jj / kRopeStages) & 1), kWaitPolls);
+    return;
+  }
+
+  // ---- consumers ----
+  const int c = threadIdx.x - 32;
+  const int v = c % nvh, r = c / nvh;
+  const bool active = r < HPL;
+  const int i0 = v * VEC;
+  int64_t j = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+    const int st = (int)(j % kRopeStages);
+    if (!mbar_wait(&full[st], (uint32_t)((j / kRopeStages) & 1), kWaitPolls)) {
+      atomicOr(err, kErrWaitTimeout);
+      break;
+    }
+    if (active) {
+      const int64_t t0 = tile * TT;
+      const int ntok = (int)(T_ - t0 < TT ? T_ - t0 : (int64_t)TT);
+      const unsigned char* base = smem + (size_t)st * g.stage;
+      const unsigned char* sq = base;
+      const unsigned char* sk = base + (size_t)TT * g.qrow;
+      const float2* scs = reinterpret_cast<const float2*>(base + g.cs_off());
+      const int* spos = reinterpret_cast<const int*>(base + g.pos_off());
+      for (int tok = 0; tok < ntok; ++tok) {
+        const int64_t t = t0 + tok;
+        const bool ok = spos[tok] >= 0;
+        const float2* cc = scs + (size_t)tok * half + i0;
+        for (int h = r; h < HT; h += HPL) {
+          const T* src = reinterpret_cast<const T*>(h < Hq ? sq + (size_t)tok * g.qrow
+                                                           : sk + (size_t)tok * g.krow) +
+                         (size_t)(h < Hq ? h : h - Hq) * D;
+          T* dst = h < Hq ? qo + ((size_t)t * Hq + h) * D : ko + ((size_t)t * Hk + (h - Hq)) * D;
+          Packed<T, VEC> a, b;
+          a.r = ld_shared_v4(src + i0);
+          b.r = ld_shared_v4(src + half + i0);
+          rotate_store<T, VEC, BWD, true>(a, b, cc, ok, dst + i0, dst + half + i0);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
   }
 }
 
@@ -215,6 +361,37 @@ gbln_status rope_typed(const void* q, const void* k, void* qo, void* ko, const i
   const int per_sm = block > 0 ? 2048 / block : 1;
   const int ut = hpt == 1 ? 2 : 1;
   const unsigned grid = grid_for((rows + ut - 1) / ut, 1, (int64_t)sms * (per_sm > 0 ? per_sm : 1));
+  // Staged (TMA bulk) path: vector layout and a token small enough that four
+  // stages of at least one token fit two blocks per SM.  In place is fine: a
+  // tile is completely in shared memory before any of its outputs is stored.
+  const size_t tok_bytes = (size_t)HT * D * sizeof(T) + (size_t)half * sizeof(float2);
+  if (vec && nvh <= 256 && tok_bytes <= kStageTarget) {
+    unsigned int* err = device_error_word();
+    if (!err) return GBLN_ERR_CUDA;
+    const int TT = (int)(kStageTarget / tok_bytes);
+    const StageGeom geo = stage_geom<T>(Hq, Hk, D, TT);
+    const size_t smem = (size_t)kRopeStages * geo.stage;
+    const int hpl = 256 / nvh < HT ? 256 / nvh : HT;
+    const int threads = 32 + ((nvh * hpl + 31) / 32) * 32;
+    auto kern = rope_staged_kernel<T, BWD>;
+    static std::atomic<uint64_t> attr_done{0};  // one bit per device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return GBLN_ERR_CUDA; }
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)(kRopeStages * (kStageTarget + 1024))) != cudaSuccess) {
+        cudaGetLastError();
+        return GBLN_ERR_CUDA;
+      }
+      attr_done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const int64_t ntiles = (rows + TT - 1) / TT;
+    const unsigned sgrid = grid_for(ntiles, 1, (int64_t)sms * 2);
+    kern<<<sgrid, threads, smem, s>>>((const T*)q, (const T*)k, (T*)qo, (T*)ko, pos,
+                                      (const float2*)cs, max_pos, rows, Hq, Hk, D, TT, hpl, err);
+    return launch_status();
+  }
   if (vec)
     rope_launch<T, VEC, BWD>(hpt, grid, block, HP, s, q, k, qo, ko, pos, cs, max_pos, rows, Hq, Hk, D);
   else

@@ -139,6 +139,10 @@ def test_swiglu_rejects(lib):
     assert lib.gbln_swiglu_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 8, F32, None) == OK
 
 
+def test_device_error_rejects_null(lib):
+    assert lib.gbln_device_error(None, 0) == INVALID
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     import rmsnorm_fwd_bwd_03_gb300 as gb

@@ -281,3 +281,19 @@ def test_swiglu_guard_bands():
     gb.swiglu_bwd(d, g, u, dgate=gdg.tensor, dup=gdu.tensor)
     torch.cuda.synchronize()
     assert go.intact() and gdg.intact() and gdu.intact()
+
+
+def test_device_error_word_is_clear_after_staged_kernels():
+    # RoPE's staged path bounds its waits on TMA copies; none may have given up.
+    T, Hq, Hk, D = 4097, 32, 8, 128
+    q = _randn((T, Hq, D), torch.bfloat16, 91)
+    k = _randn((T, Hk, D), torch.bfloat16, 92)
+    pos = torch.arange(T, dtype=torch.int32, device="cuda") % 1000
+    table = gb.rope_table(1000, D, 5e5)
+    qo, ko = gb.rope_fwd(q, k, pos, table)
+    torch.cuda.synchronize()
+    assert gb.device_error() == 0
+    p = pos.cpu().numpy()
+    rows = [0, 1, 2047, 4095, 4096]
+    check_io(to64(qo[rows]), oracle.rope_fwd(to64(q[rows]), p[rows], 5e5), "bf16", "q' staged")
+    check_io(to64(ko[rows]), oracle.rope_fwd(to64(k[rows]), p[rows], 5e5), "bf16", "k' staged")
