@@ -10,7 +10,8 @@ library's kernels, called through the C ABI with device pointers.
 Prints one JSON line.  ``value`` is tokens per second over all ranks with inputs
 resident in HBM; ``e2e`` is the same step through the same C ABI with the inputs
 in pinned host memory and the outputs read back, copies inside the timed region.
-L2 is flushed (a 2x L2 write) between timed steps.  ``--impl reference`` times
+L2 is flushed between timed steps (a 2x L2 write, then a 2x L2 read of another
+buffer, so no step data and no dirty lines remain in it).  ``--impl reference`` times
 the float64 CPU oracle on a bounded sample of the same workload instead.
 
 Multi-GPU (torchrun): each rank runs its own replica on its own batch (weak
@@ -135,12 +136,49 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+class L2Flush:
+    """Between timed steps: write a buffer of twice the L2 size (evicts the step's
+    data), then read a second one of the same size (evicts the dirty lines of the
+    write, so the next step neither finds its data in L2 nor pays for writing
+    back lines that are not its own)."""
+
+    def __init__(self, device):
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        n = max(2 * l2, 256 << 20) // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=device)
+        self.r = torch.ones(n, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
 # ---------------------------------------------------------------------------
 # The step through the C ABI
 # ---------------------------------------------------------------------------
 
+def _arena(tensors: dict, device, fill: bool):
+    """One contiguous device buffer holding every tensor (256-byte aligned views)."""
+    offs, total = {}, 0
+    for key, t in tensors.items():
+        offs[key] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    buf = torch.empty(max(total, 256), dtype=torch.uint8, device=device)
+    views = {}
+    for key, t in tensors.items():
+        nb = t.numel() * t.element_size()
+        v = buf[offs[key]:offs[key] + nb].view(t.dtype).view(t.shape)
+        if fill:
+            v.copy_(t)
+        views[key] = v
+    return buf, views
+
+
 class Step:
-    """Device buffers and the eight C-ABI calls of one fwd + bwd step."""
+    """Device buffers and the eight C-ABI calls of one fwd + bwd step.
+
+    Inputs live in one contiguous device arena and outputs in another, so that
+    the end-to-end leg moves each direction with a single copy per step."""
 
     def __init__(self, wl, device, seed):
         import rmsnorm_fwd_bwd_03_gb300 as gb
@@ -149,18 +187,22 @@ class Step:
         self.lib = gb.library()
         self.wl = wl
         T, H = wl.T, wl.H
-        inp = make_inputs(wl, device, seed=seed)
-        self.inp = inp
-        e = lambda like: torch.empty_like(like)  # noqa: E731
-        self.out = {
-            "positions": torch.empty(T, dtype=torch.int32, device=device),
-            "y": e(inp["x"]), "h": e(inp["x"]),
-            "rstd": torch.empty(T, dtype=torch.float32, device=device),
-            "q_out": e(inp["q"]), "k_out": e(inp["k"]),
-            "out": e(inp["gate"]), "dgate": e(inp["gate"]), "dup": e(inp["up"]),
-            "dq_in": e(inp["dq"]), "dk_in": e(inp["dk"]),
-            "dx": e(inp["x"]), "dw": torch.empty(H, dtype=torch.float32, device=device),
+        gen = make_inputs(wl, device, seed=seed)
+        self.in_arena, self.inp = _arena(gen, device, fill=True)
+        del gen
+        i = self.inp
+        meta = lambda shape, dt: torch.empty(shape, dtype=dt, device="meta")  # noqa: E731  (shape/dtype only)
+        like = lambda t: meta(t.shape, t.dtype)  # noqa: E731
+        spec = {
+            "positions": meta((T,), torch.int32),
+            "y": like(i["x"]), "h": like(i["x"]),
+            "rstd": meta((T,), torch.float32),
+            "q_out": like(i["q"]), "k_out": like(i["k"]),
+            "out": like(i["gate"]), "dgate": like(i["gate"]), "dup": like(i["up"]),
+            "dq_in": like(i["dq"]), "dk_in": like(i["dk"]),
+            "dx": like(i["x"]), "dw": meta((H,), torch.float32),
         }
+        self.out_arena, self.out = _arena(spec, device, fill=False)
         self.P = gb.rmsnorm_bwd_num_partials(T, H, wl.dtype)
         self.partial = torch.empty((self.P, H), dtype=torch.float32, device=device)
         self.max_pos = wl.max_pos()
@@ -196,11 +238,61 @@ class Step:
              (p(self.partial), self.P, H, p(o["dw"]), 0, s)),
         ]
 
-    def host_io(self):
-        """Pinned host copies of the step's inputs and outputs (for the end-to-end leg)."""
-        ins = {k: v.cpu().pin_memory() for k, v in self.inp.items()}
-        outs = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in self.out.items()}
-        return ins, outs
+
+def e2e_pipelined(wl, device, steps, warmup, world, seed):
+    """Throughput of the step with inputs in pinned host memory and every output
+    read back: per step one host-to-device copy of the input arena, the eight
+    C-ABI calls, and one device-to-host copy of the output arena.  Two device
+    buffer sets and three streams overlap step i's kernels with step i+1's
+    upload and step i-1's download; every step's copies are inside the timed
+    region."""
+    sets = [Step(wl, device, seed), Step(wl, device, seed)]
+    host_in = sets[0].in_arena.cpu().pin_memory()
+    host_out = [torch.empty(st.out_arena.shape, dtype=torch.uint8, pin_memory=True) for st in sets]
+    s_in, s_comp, s_out = (torch.cuda.Stream(device) for _ in range(3))
+    calls = [st.calls(s_comp.cuda_stream) for st in sets]
+    ev_in = [torch.cuda.Event() for _ in sets]
+    ev_comp = [torch.cuda.Event() for _ in sets]
+    ev_out = [torch.cuda.Event() for _ in sets]
+
+    def run(n):
+        for it in range(n):
+            b = it % 2
+            with torch.cuda.stream(s_in):
+                if it >= 2:
+                    s_in.wait_event(ev_comp[b])  # step it-2 has finished reading set b
+                sets[b].in_arena.copy_(host_in, non_blocking=True)
+                ev_in[b].record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(ev_in[b])
+                if it >= 2:
+                    s_comp.wait_event(ev_out[b])  # step it-2's outputs have been read back
+                run_calls(calls[b])
+                ev_comp[b].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[b])
+                host_out[b].copy_(sets[b].out_arena, non_blocking=True)
+                ev_out[b].record(s_out)
+
+    run(warmup)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    run(steps)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_comp)
+    e1.record(s_out)
+    torch.cuda.synchronize()
+    ms = reduce_max(e0.elapsed_time(e1), world)
+    h2d = sets[0].in_arena.numel()
+    d2h = sets[0].out_arena.numel()
+    return {"value": world * wl.T * steps / (ms * 1e-3), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "ms_per_step": ms / steps,
+            "method": "one pinned H2D copy of the input arena, the 8 C-ABI calls and one D2H "
+                      "copy of the output arena per step; copies on their own streams overlap "
+                      "the neighbouring steps' kernels (two device buffer sets)"}
 
 
 def run_calls(calls, events=None):
@@ -278,15 +370,14 @@ def run_single_op(args, wl, device):
     calls = step.calls(stream.cuda_stream)
     run_calls(calls)  # every output of the step exists (h, rstd, positions, partials)
     call = [c for c in calls if c[0] == args.op]
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(device)
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         run_calls(call)
     torch.cuda.synchronize()
     times = []
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(call) + 1)]
         run_calls(call, ev)
         times.append(ev)
@@ -331,6 +422,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the step as eight eager launches instead of one CUDA graph replay")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--op", choices=OPS, default=None,
                     help="time one operator alone (also the driver for ncu captures)")
@@ -351,7 +444,8 @@ def main():
               "heads_q": wl.Hq, "heads_kv": wl.Hk, "head_dim": wl.D, "intermediate": wl.I,
               "rope_theta": wl.theta, "eps": wl.eps, "fused_residual": wl.residual,
               "global_batch_tokens": wl.T * world, "parallelism": f"replicas x{world}",
-              "l2": "flushed between timed steps (write of 2x L2 size)"}
+              "l2": "flushed between timed steps: 2x L2 written, then 2x L2 of another buffer read "
+                    "(no step data and no dirty lines left in L2)"}
 
     if args.impl == "reference":
         if rank != 0:
@@ -389,49 +483,83 @@ def main():
     step = Step(wl, device, seed=rank)
     stream = torch.cuda.current_stream(device)
     calls = step.calls(stream.cuda_stream)
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(device)
 
     nk = len(calls)
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         run_calls(calls)
     torch.cuda.synchronize()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    # The step as one CUDA graph of the eight C-ABI calls (captured once, replayed
+    # per step): the launch path a training loop would use.
+    graph = None
+    if not args.eager:
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            run_calls(step.calls(torch.cuda.current_stream(device).cuda_stream))
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            flush()
+            graph.replay()
+        torch.cuda.synchronize()
+
+    # Timed region 1 (the headline): K steps, events around each step, L2 flushed between.
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t_wall0 = time.perf_counter()
         for k in range(args.steps):
-            flush.zero_()
-            run_calls(calls, evs[k])
+            flush()
+            evs[k][0].record()
+            if graph is not None:
+                graph.replay()
+            else:
+                run_calls(calls)
+            evs[k][1].record()
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
     barrier(world)
-
-    per_op = {name: 0.0 for name, _, _ in calls}
-    step_ms = []
-    for k in range(args.steps):
-        e = evs[k]
-        step_ms.append(e[0].elapsed_time(e[nk]))
-        for j, (name, _, _) in enumerate(calls):
-            per_op[name] += e[j].elapsed_time(e[j + 1])
-    total_ms = sum(step_ms)
+    total_ms = sum(a.elapsed_time(b) for a, b in evs)
     total_ms_max = reduce_max(total_ms, world)
     ms_per_step = total_ms_max / args.steps
     value = world * wl.T * args.steps / (total_ms_max * 1e-3)
+
+    # Timed region 2 (per-kernel durations for the roofline): eager steps with an
+    # event between consecutive kernels on the launching stream.  Each interval
+    # also holds that launch's front-end overhead, so these durations are upper
+    # bounds and the GB/s derived from them lower bounds.
+    kb = max(3, min(args.steps, 200))
+    kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(kb)]
+    torch.cuda.synchronize()
+    for k in range(kb):
+        flush()
+        run_calls(calls, kevs[k])
+    torch.cuda.synchronize()
+    per_op = {name: 0.0 for name, _, _ in calls}
+    eager_ms = 0.0
+    for k in range(kb):
+        e = kevs[k]
+        eager_ms += e[0].elapsed_time(e[nk])
+        for j, (name, _, _) in enumerate(calls):
+            per_op[name] += e[j].elapsed_time(e[j + 1])
+    for name in per_op:
+        per_op[name] = reduce_max(per_op[name], world)
 
     alg = wl.algorithmic_bytes()
     peak, peak_kind = _measured_peak()
     kernels = {}
     for name in per_op:
-        ms = per_op[name] / args.steps
+        ms = per_op[name] / kb
         gbs = alg[name] / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
         kernels[name] = {"ms": round(ms, 5), "alg_bytes": alg[name], "GB/s": round(gbs, 1),
                          "frac_of_peak": round(gbs / peak, 4)}
     dom = max(per_op, key=per_op.get)
-    dom_ms = per_op[dom] / args.steps
+    dom_ms = per_op[dom] / kb
     achieved = alg[dom] / (dom_ms * 1e-3) / 1e9
     tr = NCU_TRAFFIC.get((wl.name, dom))
     traffic = tr["bytes"] if tr and tr.get("src_sha") == _src_sha(dom) else None
@@ -450,36 +578,16 @@ def main():
             "frac_of_peak_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4),
             "roofline": roofline, "kernels": kernels,
             "gpu_launches": nk * args.steps,
+            "launch": "eager C-ABI calls" if graph is None else "CUDA graph of the 8 C-ABI calls, one replay per step",
+            "per_kernel_region": {"steps": kb, "launch": "eager, event between kernels",
+                                  "ms_per_step": round(eager_ms / kb, 5), "gpu_launches": nk * kb},
             "wall_s_timed_region": round(t_wall, 3),
             "clocks": clk.summary()}
 
     if not args.no_e2e:
-        ins, outs = step.host_io()
-        h2d = sum(v.numel() * v.element_size() for v in ins.values())
-        d2h = sum(v.numel() * v.element_size() for v in outs.values())
-        dev_in = step.inp
+        del graph
         ksteps = max(3, min(args.steps, 50))
-
-        def e2e_step():
-            for key, hv in ins.items():
-                dev_in[key].copy_(hv, non_blocking=True)
-            run_calls(calls)
-            for key, hv in outs.items():
-                hv.copy_(step.out[key], non_blocking=True)
-        for _ in range(args.warmup):
-            e2e_step()
-        torch.cuda.synchronize()
-        barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(ksteps):
-            e2e_step()
-        e1.record()
-        torch.cuda.synchronize()
-        e2e_ms = reduce_max(e0.elapsed_time(e1), world)
-        line["e2e"] = {"value": world * wl.T * ksteps / (e2e_ms * 1e-3), "unit": "tokens/s",
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ksteps,
-                       "ms_per_step": e2e_ms / ksteps}
+        line["e2e"] = e2e_pipelined(wl, device, ksteps, args.warmup, world, seed=rank)
         line["gpu_launches_e2e"] = nk * ksteps
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

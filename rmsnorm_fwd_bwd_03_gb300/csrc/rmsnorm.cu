@@ -296,12 +296,12 @@ rms_bwd_generic(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
 }
 
 // ---------------------------------------------------------------------------
-// Finalize: dw[j] = (acc ? dw[j] : 0) + sum_p partial[p, j].  Block (32, 16):
-// column j = 32 * blockIdx.x + tx; row stripe ty sums p = ty, ty + 16, ... in
+// Finalize: dw[j] = (acc ? dw[j] : 0) + sum_p partial[p, j].  Block (32, 32):
+// column j = 32 * blockIdx.x + tx; row stripe ty sums p = ty, ty + 32, ... in
 // order (loads unrolled so several are in flight; the additions stay in that
-// order), then the 16 stripes are added in order.  Bitwise reproducible.
+// order), then the 32 stripes are added in order.  Bitwise reproducible.
 // ---------------------------------------------------------------------------
-constexpr int kFinStripes = 16;
+constexpr int kFinStripes = 32;
 
 __global__ void __launch_bounds__(32 * kFinStripes)
 rms_dw_finalize(const float* __restrict__ partial, int64_t P, int H, float* dw, int accumulate) {

@@ -308,17 +308,28 @@ __global__ void rope_table_kernel(float2* cs, int64_t max_pos, int half, int D, 
   }
 }
 
-// positions[t] = t - cu[d] for cu[d] <= t < cu[d+1]; binary search per token.
-__global__ void positions_kernel(const int32_t* __restrict__ cu, int ndoc, int32_t* pos,
-                                 int64_t T_) {
+// positions[t] = t - cu[d] for cu[d] <= t < cu[d+1]: binary search per token
+// over the document boundaries, staged in shared memory when they fit (one
+// coalesced read per block instead of a chain of dependent global loads).
+constexpr int kPosSmemDocs = 4096;
+
+__global__ void __launch_bounds__(256)
+positions_kernel(const int32_t* __restrict__ cu, int ndoc, int32_t* pos, int64_t T_) {
+  __shared__ int32_t scu[kPosSmemDocs];
+  const bool staged = ndoc <= kPosSmemDocs;
+  if (staged) {
+    for (int i = threadIdx.x; i < ndoc; i += blockDim.x) scu[i] = __ldg(cu + i);
+    __syncthreads();
+  }
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T_;
        t += (int64_t)gridDim.x * blockDim.x) {
     int lo = 0, hi = ndoc - 1;  // largest d in [0, ndoc) with cu[d] <= t
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if ((int64_t)__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+      const int32_t c = staged ? scu[mid] : __ldg(cu + mid);
+      if ((int64_t)c <= t) lo = mid; else hi = mid - 1;
     }
-    pos[t] = (int32_t)(t - (int64_t)__ldg(cu + lo));
+    pos[t] = (int32_t)(t - (int64_t)(staged ? scu[lo] : __ldg(cu + lo)));
   }
 }
 
@@ -458,7 +469,7 @@ extern "C" gbln_status gbln_positions_from_cu_seqlens(const int32_t* cu_seqlens,
   if (!positions || T < 0 || T > (1LL << 31) - 1 || ndoc < 0) return GBLN_ERR_INVALID_ARG;
   if (T == 0) return GBLN_OK;
   if (!cu_seqlens || ndoc < 1) return GBLN_ERR_INVALID_ARG;  // tokens need a document
-  positions_kernel<<<grid_for(T, 256, 8192), 256, 0, (cudaStream_t)stream>>>(cu_seqlens, ndoc,
+  positions_kernel<<<grid_for(T, 256, 1024), 256, 0, (cudaStream_t)stream>>>(cu_seqlens, ndoc,
                                                                                positions, T);
   return launch_status();
 }
