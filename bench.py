@@ -42,7 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 OPS = ["positions", "rmsnorm_fwd", "rope_fwd", "swiglu_fwd", "swiglu_bwd", "rope_bwd",
        "rmsnorm_bwd", "rmsnorm_dw_finalize"]
 KERNEL_SOURCE = {"positions": "rope.cu", "rmsnorm_fwd": "rmsnorm.cu", "rope_fwd": "rope.cu",
-                 "swiglu_fwd": "swiglu.cu", "swiglu_bwd": "swiglu.cu", "rope_bwd": "rope.cu",
+                 "swiglu_fwd": "glu.cu", "swiglu_bwd": "glu.cu", "rope_bwd": "rope.cu",
                  "rmsnorm_bwd": "rmsnorm.cu", "rmsnorm_dw_finalize": "rmsnorm.cu"}
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by workload and
 # operator, with the sha256 of the kernel source they were taken on: a changed

@@ -63,6 +63,14 @@ typedef enum {
 
 typedef enum { GBLN_F32 = 0, GBLN_BF16 = 1 } gbln_dtype;
 
+/* Activation of the gated and plain MLP units ([FL] 支持的 MLP 变体: SiLU / GeLU / ReLU). */
+typedef enum {
+  GBLN_ACT_SILU = 0,      /* x / (1 + exp(-x))                                    */
+  GBLN_ACT_GELU_TANH = 1, /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))       */
+  GBLN_ACT_GELU_ERF = 2,  /* 0.5 x (1 + erf(x / sqrt(2)))  (exact GeLU)             */
+  GBLN_ACT_RELU = 3       /* max(x, 0); derivative 1 for x > 0, else 0              */
+} gbln_act;
+
 /* Human-readable name of a status code.  Never NULL; the string is static. */
 const char* gbln_status_string(int status);
 
@@ -220,6 +228,35 @@ gbln_status gbln_rope_bwd(const void* dq, const void* dk, void* dq_in, void* dk_
                           int64_t T, int32_t Hq, int32_t Hk, int32_t D,
                           gbln_dtype io, gbln_stream_t stream);
 
+/* Pairing of the rotated elements. */
+typedef enum {
+  GBLN_ROPE_HALF = 0,       /* (i, i + D/2): the default rotary type (gbln_rope_fwd)   */
+  GBLN_ROPE_INTERLEAVED = 1 /* (2i, 2i + 1), frequency index i                        */
+} gbln_rope_pairing;
+
+/*
+ * gbln_rope_fwd with strided rows and a choice of pairing: head row h of token t
+ * of q starts at q + t * ld_q + h * D (elements), likewise for k, q_out, k_out
+ * (ld_q, ld_q_out >= Hq * D; ld_k, ld_k_out >= Hk * D).  Q and K can thus be read
+ * from, and written back into, one packed [T, (Hq + 2 Hk) * D] QKV projection
+ * output (q = qkv, k = qkv + Hq * D, every ld = (Hq + 2 Hk) * D; in place with
+ * q_out = q, k_out = k).  Interleaved pairing rotates elements (2i, 2i + 1) by
+ * pos * theta^(-2i/D) with the same cos/sin table.  Errors as gbln_rope_fwd, plus
+ * INVALID_ARG for a stride below its row width or an unknown pairing.
+ */
+gbln_status gbln_rope_fwd_ex(const void* q, const void* k, void* q_out, void* k_out,
+                             const int32_t* positions, const float* cos_sin, int64_t max_pos,
+                             int64_t T, int32_t Hq, int32_t Hk, int32_t D, int64_t ld_q,
+                             int64_t ld_k, int64_t ld_q_out, int64_t ld_k_out,
+                             gbln_rope_pairing pairing, gbln_dtype io, gbln_stream_t stream);
+
+/* Backward of gbln_rope_fwd_ex (inverse rotation), same layout arguments. */
+gbln_status gbln_rope_bwd_ex(const void* dq, const void* dk, void* dq_in, void* dk_in,
+                             const int32_t* positions, const float* cos_sin, int64_t max_pos,
+                             int64_t T, int32_t Hq, int32_t Hk, int32_t D, int64_t ld_dq,
+                             int64_t ld_dk, int64_t ld_dq_in, int64_t ld_dk_in,
+                             gbln_rope_pairing pairing, gbln_dtype io, gbln_stream_t stream);
+
 /*
  * Positions of packed documents: positions[t] = t - cu_seqlens[d] for the document
  * d with cu_seqlens[d] <= t < cu_seqlens[d+1] ([FL] 训练配置示例: micro-batches
@@ -254,6 +291,41 @@ gbln_status gbln_swiglu_fwd(const void* gate, const void* up, void* out,
 gbln_status gbln_swiglu_bwd(const void* dout, const void* gate, const void* up,
                             void* dgate, void* dup,
                             int64_t T, int64_t I, gbln_dtype io, gbln_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Gated units with any activation and row strides; plain activations          */
+/* ([FL] 支持的 MLP 变体: dense MLP gated or not, SiLU / GeLU / ReLU)           */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * out[t, j] = f(gate[t, j]) * up[t, j] for t < T, j < I, f = act (see gbln_act).
+ * Row t of each tensor starts ld elements after row t - 1 (ld >= I), so gate and
+ * up may be the two halves of one packed [T, 2I] projection output
+ * (gate = p, up = p + I, ld_gate = ld_up = 2I).  With every ld = I and
+ * act = GBLN_ACT_SILU this is gbln_swiglu_fwd.  out may alias gate or up exactly.
+ * Errors: INVALID_ARG for a bad act, T < 0, I <= 0, ld < I, null pointers (T > 0).
+ */
+gbln_status gbln_glu_fwd(const void* gate, const void* up, void* out, int64_t T, int64_t I,
+                         int64_t ld_gate, int64_t ld_up, int64_t ld_out, gbln_act act,
+                         gbln_dtype io, gbln_stream_t stream);
+
+/*
+ * dgate = dout * up * f'(gate), dup = dout * f(gate), each with its own row
+ * stride (a packed [T, 2I] gradient: dgate = q, dup = q + I, ld = 2I).  dgate may
+ * alias gate and dup may alias up exactly.  Errors as gbln_glu_fwd.
+ */
+gbln_status gbln_glu_bwd(const void* dout, const void* gate, const void* up, void* dgate,
+                         void* dup, int64_t T, int64_t I, int64_t ld_dout, int64_t ld_gate,
+                         int64_t ld_up, int64_t ld_dgate, int64_t ld_dup, gbln_act act,
+                         gbln_dtype io, gbln_stream_t stream);
+
+/* y = f(x) over n contiguous elements (non-gated MLP); y may alias x. */
+gbln_status gbln_act_fwd(const void* x, void* y, int64_t n, gbln_act act, gbln_dtype io,
+                         gbln_stream_t stream);
+
+/* dx = dy * f'(x) over n contiguous elements; dx may alias dy or x. */
+gbln_status gbln_act_bwd(const void* dy, const void* x, void* dx, int64_t n, gbln_act act,
+                         gbln_dtype io, gbln_stream_t stream);
 
 #ifdef __cplusplus
 }

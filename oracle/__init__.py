@@ -38,6 +38,8 @@ Pins for every function live in ``tests/test_oracle_pins.py``.
 
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 __all__ = [
@@ -53,6 +55,11 @@ __all__ = [
     "silu",
     "swiglu_fwd",
     "swiglu_bwd",
+    "ACTIVATIONS",
+    "act",
+    "act_grad",
+    "glu_fwd",
+    "glu_bwd",
     "positions_from_doc_lengths",
     "positions_from_cu_seqlens",
 ]
@@ -172,7 +179,7 @@ def rope_inv_freq(D, theta):
     return np.power(float(theta), -2.0 * i / D)
 
 
-def _rope_rotate(x, positions, theta, sign):
+def _rope_rotate(x, positions, theta, sign, pairing="half"):
     x = np.asarray(x, dtype=np.float64)
     D = x.shape[-1]
     half = D // 2
@@ -180,26 +187,40 @@ def _rope_rotate(x, positions, theta, sign):
     angle = np.asarray(positions, dtype=np.float64)[:, None] * freq  # [T, D/2]
     cos = np.cos(angle)[:, None, :]                                 # [T, 1, D/2]
     sin = sign * np.sin(angle)[:, None, :]
-    x1 = x[..., :half]
-    x2 = x[..., half:]
+    if pairing == "half":          # pair (i, i + D/2)
+        x1 = x[..., :half]
+        x2 = x[..., half:]
+    elif pairing == "interleaved":  # pair (2i, 2i + 1)
+        x1 = x[..., 0::2]
+        x2 = x[..., 1::2]
+    else:
+        raise ValueError(pairing)
+    y1 = x1 * cos - x2 * sin
+    y2 = x2 * cos + x1 * sin
     out = np.empty_like(x)
-    out[..., :half] = x1 * cos - x2 * sin
-    out[..., half:] = x2 * cos + x1 * sin
+    if pairing == "half":
+        out[..., :half] = y1
+        out[..., half:] = y2
+    else:
+        out[..., 0::2] = y1
+        out[..., 1::2] = y2
     return out
 
 
-def rope_fwd(x, positions, theta):
-    """Rotate every head of token t by angle ``positions[t] * theta_i`` on pair (i, i + D/2).
+def rope_fwd(x, positions, theta, pairing="half"):
+    """Rotate every head of token t by angle ``positions[t] * theta_i`` on pair i.
 
-    x: [T, heads, D] float64; positions: [T] integers.  Returns the rotated
-    array.  Q and K are each passed through this with the same positions.
+    x: [T, heads, D] float64; positions: [T] integers.  ``pairing`` "half" pairs
+    element i with i + D/2 (the default rotary type); "interleaved" pairs 2i
+    with 2i + 1.  Returns the rotated array.  Q and K are each passed through this
+    with the same positions.
     """
-    return _rope_rotate(x, positions, theta, +1.0)
+    return _rope_rotate(x, positions, theta, +1.0, pairing)
 
 
-def rope_bwd(dout, positions, theta):
+def rope_bwd(dout, positions, theta, pairing="half"):
     """Gradient of :func:`rope_fwd`: the transpose (= inverse) rotation, angle negated."""
-    return _rope_rotate(dout, positions, theta, -1.0)
+    return _rope_rotate(dout, positions, theta, -1.0, pairing)
 
 
 # ---------------------------------------------------------------------------
@@ -239,6 +260,67 @@ def swiglu_bwd(dout, gate, up):
     dgate = dout * u * s * (1.0 + g * (1.0 - s))
     dup = dout * g * s
     return dgate, dup
+
+
+# ---------------------------------------------------------------------------
+# Gated and plain MLP activations ("Fast-LLM: 高效大语言模型训练框架", §三 支持的 MLP
+# 变体: dense MLP gated or not, with SiLU / GeLU / ReLU).  GeLU comes in its exact
+# form x * Phi(x) (Phi the standard normal CDF, via erf) and in the common tanh
+# approximation 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+# ---------------------------------------------------------------------------
+
+ACTIVATIONS = ("silu", "gelu_tanh", "gelu_erf", "relu")
+
+_SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
+
+
+def act(name, x):
+    """Activation value f(x)."""
+    x = np.asarray(x, dtype=np.float64)
+    if name == "silu":
+        return silu(x)
+    if name == "gelu_tanh":
+        return 0.5 * x * (1.0 + np.tanh(_SQRT_2_OVER_PI * (x + 0.044715 * x ** 3)))
+    if name == "gelu_erf":
+        return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))
+    if name == "relu":
+        return np.maximum(x, 0.0)
+    raise ValueError(name)
+
+
+def act_grad(name, x):
+    """Derivative f'(x) (for ReLU: 1 where x > 0, else 0)."""
+    x = np.asarray(x, dtype=np.float64)
+    if name == "silu":
+        s = _sigmoid(x)
+        return s * (1.0 + x * (1.0 - s))
+    if name == "gelu_tanh":
+        z = _SQRT_2_OVER_PI * (x + 0.044715 * x ** 3)
+        t = np.tanh(z)
+        dz = _SQRT_2_OVER_PI * (1.0 + 3.0 * 0.044715 * x ** 2)
+        return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * dz
+    if name == "gelu_erf":
+        pdf = np.exp(-0.5 * x * x) / math.sqrt(2.0 * math.pi)
+        return 0.5 * (1.0 + _erf(x / math.sqrt(2.0))) + x * pdf
+    if name == "relu":
+        return (x > 0).astype(np.float64)
+    raise ValueError(name)
+
+
+def _erf(x):
+    from scipy.special import erf  # library primitive for the normal CDF
+    return erf(x)
+
+
+def glu_fwd(name, gate, up):
+    """Gated unit ``out = f(gate) * up`` (SwiGLU is f = SiLU)."""
+    return act(name, gate) * np.asarray(up, dtype=np.float64)
+
+
+def glu_bwd(name, dout, gate, up):
+    """Gradients of :func:`glu_fwd`: ``dgate = dout * up * f'(gate)``, ``dup = dout * f(gate)``."""
+    dout = np.asarray(dout, dtype=np.float64)
+    return dout * np.asarray(up, dtype=np.float64) * act_grad(name, gate), dout * act(name, gate)
 
 
 # ---------------------------------------------------------------------------

@@ -21,13 +21,15 @@ __all__ = [
     "GblnError", "library", "library_path", "status_string", "version", "device_error",
     "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_num_partials", "rmsnorm_dw_finalize",
     "rmsnorm_bwd_noalloc",
-    "rope_table", "rope_fwd", "rope_bwd", "positions_from_cu_seqlens",
-    "swiglu_fwd", "swiglu_bwd",
+    "rope_table", "rope_fwd", "rope_bwd", "rope_fwd_ex", "rope_bwd_ex", "positions_from_cu_seqlens",
+    "swiglu_fwd", "swiglu_bwd", "glu_fwd", "glu_bwd", "act_fwd", "act_bwd", "ACT",
     "F32", "BF16",
 ]
 
 F32 = 0
 BF16 = 1
+# gbln_act
+ACT = {"silu": 0, "gelu_tanh": 1, "gelu_erf": 2, "relu": 3}
 _DTYPE = {torch.float32: F32, torch.bfloat16: BF16}
 
 _vp = ctypes.c_void_p
@@ -49,9 +51,15 @@ _SIGNATURES = {
     "gbln_rope_table": (ctypes.c_int, [_vp, _i64, _i32, _f64, _vp]),
     "gbln_rope_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, ctypes.c_int, _vp]),
     "gbln_rope_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, ctypes.c_int, _vp]),
+    "gbln_rope_fwd_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
+    "gbln_rope_bwd_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
     "gbln_positions_from_cu_seqlens": (ctypes.c_int, [_vp, _i32, _vp, _i64, _vp]),
     "gbln_swiglu_fwd": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp]),
     "gbln_swiglu_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp]),
+    "gbln_glu_fwd": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
+    "gbln_glu_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
+    "gbln_act_fwd": (ctypes.c_int, [_vp, _vp, _i64, ctypes.c_int, ctypes.c_int, _vp]),
+    "gbln_act_bwd": (ctypes.c_int, [_vp, _vp, _vp, _i64, ctypes.c_int, ctypes.c_int, _vp]),
 }
 
 _lib = None
@@ -256,6 +264,53 @@ def rope_bwd(dq, dk, positions, cos_sin, *, dq_in=None, dk_in=None):
     return _rope("gbln_rope_bwd", dq, dk, positions, cos_sin, dq_in, dk_in)
 
 
+PAIRING = {"half": 0, "interleaved": 1}
+
+
+def _heads(t, name):
+    """(T, H, D, token stride) of a [T, H, D] view whose heads are contiguous in each token row."""
+    if t is None:
+        return 0, 0, 0, 0
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != 3 or t.stride(2) != 1 or (t.shape[1] > 1 and t.stride(1) != t.shape[2]):
+        raise ValueError(f"{name} must be [T, H, D] with contiguous heads in each token row")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
+    T, H, D = t.shape
+    return T, H, D, (t.stride(0) if T > 1 else H * D)
+
+
+def _rope_ex(name, q, k, positions, cos_sin, q_out, k_out, pairing):
+    T, Hq, D, ldq = _heads(q, "q")
+    _, Hk, _, ldk = _heads(k, "k")
+    if q_out is None:
+        q_out = torch.empty((T, Hq, D), dtype=q.dtype, device=q.device)
+    if k is not None and k_out is None:
+        k_out = torch.empty((T, Hk, D), dtype=k.dtype, device=k.device)
+    _, _, _, ldqo = _heads(q_out, "q_out")
+    _, _, _, ldko = _heads(k_out, "k_out")
+    st = getattr(library(), name)(
+        q.data_ptr(), None if k is None else k.data_ptr(), q_out.data_ptr(),
+        None if k_out is None else k_out.data_ptr(), _dev(positions, "positions"),
+        _dev(cos_sin, "cos_sin"), cos_sin.shape[0], T, Hq, Hk, D, ldq, ldk, ldqo, ldko,
+        PAIRING[pairing], _io(q), _stream(q))
+    _check(name, st)
+    return q_out, k_out
+
+
+def rope_fwd_ex(q, k, positions, cos_sin, *, q_out=None, k_out=None, pairing="half"):
+    """``gbln_rope_fwd_ex``: like :func:`rope_fwd` on [T, H, D] views whose token rows may
+    be strided (e.g. slices of one packed QKV tensor), with ``pairing`` "half" or
+    "interleaved".  Pass ``q_out=q, k_out=k`` to rotate in place."""
+    return _rope_ex("gbln_rope_fwd_ex", q, k, positions, cos_sin, q_out, k_out, pairing)
+
+
+def rope_bwd_ex(dq, dk, positions, cos_sin, *, dq_in=None, dk_in=None, pairing="half"):
+    """``gbln_rope_bwd_ex``: inverse rotation of :func:`rope_fwd_ex`."""
+    return _rope_ex("gbln_rope_bwd_ex", dq, dk, positions, cos_sin, dq_in, dk_in, pairing)
+
+
 def positions_from_cu_seqlens(cu_seqlens, T: int, out=None):
     """``gbln_positions_from_cu_seqlens``: int32 [T] position of each token in its document."""
     if cu_seqlens.dtype != torch.int32:
@@ -302,3 +357,74 @@ def swiglu_bwd(dout, gate, up, dgate=None, dup=None):
                                    _stream(gate))
     _check("gbln_swiglu_bwd", st)
     return dgate, dup
+
+
+# ---------------------------------------------------------------------------
+# Gated units with any activation and row strides; plain activations
+# ---------------------------------------------------------------------------
+
+def _rows2d(t, name):
+    """(T, I, ld) of a 2-D view whose rows may be strided (last dim contiguous)."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with contiguous rows")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
+    return t.shape[0], t.shape[1], t.stride(0) if t.shape[0] > 1 else t.shape[1]
+
+
+def glu_fwd(gate, up, act="silu", out=None):
+    """``gbln_glu_fwd``: f(gate) * up on [T, I] views whose rows may be strided
+    (e.g. ``gate, up = packed.chunk(2, dim=-1)`` of a [T, 2I] tensor)."""
+    T, I, ldg = _rows2d(gate, "gate")
+    _, _, ldu = _rows2d(up, "up")
+    if up.shape != gate.shape or up.dtype != gate.dtype:
+        raise ValueError("gate and up must have the same shape and dtype")
+    if out is None:
+        out = torch.empty((T, I), dtype=gate.dtype, device=gate.device)
+    _, _, ldo = _rows2d(out, "out")
+    st = library().gbln_glu_fwd(gate.data_ptr(), up.data_ptr(), out.data_ptr(), T, I, ldg, ldu, ldo,
+                                ACT[act], _io(gate), _stream(gate))
+    _check("gbln_glu_fwd", st)
+    return out
+
+
+def glu_bwd(dout, gate, up, act="silu", dgate=None, dup=None):
+    """``gbln_glu_bwd``.  Returns ``(dgate, dup)``; pass views of one [T, 2I] tensor
+    as ``dgate``/``dup`` to get the packed gradient of a fused projection."""
+    T, I, ldd = _rows2d(dout, "dout")
+    _, _, ldg = _rows2d(gate, "gate")
+    _, _, ldu = _rows2d(up, "up")
+    if not (dout.shape == gate.shape == up.shape) or not (dout.dtype == gate.dtype == up.dtype):
+        raise ValueError("dout, gate and up must have the same shape and dtype")
+    if dgate is None:
+        dgate = torch.empty((T, I), dtype=gate.dtype, device=gate.device)
+    if dup is None:
+        dup = torch.empty((T, I), dtype=gate.dtype, device=gate.device)
+    _, _, lddg = _rows2d(dgate, "dgate")
+    _, _, lddu = _rows2d(dup, "dup")
+    st = library().gbln_glu_bwd(dout.data_ptr(), gate.data_ptr(), up.data_ptr(), dgate.data_ptr(),
+                                dup.data_ptr(), T, I, ldd, ldg, ldu, lddg, lddu, ACT[act], _io(gate),
+                                _stream(gate))
+    _check("gbln_glu_bwd", st)
+    return dgate, dup
+
+
+def act_fwd(x, act="silu", out=None):
+    """``gbln_act_fwd``: f(x) elementwise on a contiguous tensor."""
+    if out is None:
+        out = torch.empty_like(x)
+    st = library().gbln_act_fwd(_dev(x, "x"), _dev(out, "out"), x.numel(), ACT[act], _io(x), _stream(x))
+    _check("gbln_act_fwd", st)
+    return out
+
+
+def act_bwd(dy, x, act="silu", dx=None):
+    """``gbln_act_bwd``: dy * f'(x) elementwise on contiguous tensors."""
+    if dx is None:
+        dx = torch.empty_like(x)
+    st = library().gbln_act_bwd(_dev(dy, "dy"), _dev(x, "x"), _dev(dx, "dx"), x.numel(), ACT[act], _io(x),
+                                _stream(x))
+    _check("gbln_act_bwd", st)
+    return dx

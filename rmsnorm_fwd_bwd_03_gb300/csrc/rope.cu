@@ -5,14 +5,14 @@
 // "训练配置示例" (rotary type default, theta; heads / head_groups / head_size for
 // grouped-query attention; micro_batch_size in tokens with
 // maximum_document_length); "LLaMA-Factory Kernels 系统" (fused RoPE).
-// Pairing is rotate-half: element i turns with element i + D/2.
+// Default pairing is rotate-half (element i turns with element i + D/2); the
+// interleaved pairing (2i with 2i + 1) is the other common rotary type.
+// Q and K may sit in strided rows (e.g. inside one packed QKV projection output).
 //
-// HBM-bound design: one thread moves the two 16-byte vectors at i and i + D/2
-// of a head row, so each element is read and written exactly once (in place is
-// allowed).  A block covers all heads of a few consecutive tokens at a time;
-// each thread reads a token's position and its slice of the cos/sin row
-// (float32, from a table built once in double precision, served from L1 / L2)
-// once and applies it to every head it owns.  No integer division in the loop.
+// HBM-bound design: each element is read and written exactly once (in place is
+// allowed); cos/sin come from a float32 table built once in double precision.
+// The main path is a warp-specialised TMA pipeline (see rope_staged_kernel);
+// a register path covers layouts it does not take.
 
 #include <atomic>
 
@@ -96,27 +96,71 @@ __device__ __forceinline__ void rotate_store(const Packed<T, VEC>& a, const Pack
   }
 }
 
-// Block of HP * NVH threads, NVH = D/2/VEC vectors per half head row: thread
-// (hl, v) owns vector v (elements v*VEC.. and D/2 + v*VEC..) of heads hl,
-// hl + HP, ... (HPT of them per pass) of UT consecutive tokens per iteration;
-// token groups are strided by gridDim.  All UT * HPT head loads are issued
-// before the first is used, and they do not wait on the position -> cos/sin
-// lookup, which is served from L1 / L2 and reused across the thread's heads.
-template <typename T, int VEC, bool BWD, int HPT, int UT>
+// Interleaved pairing: one vector of N elements holds N/2 pairs (2m, 2m + 1),
+// rotated with cos/sin entries c[0..N/2).
+template <typename T, int N, bool BWD, bool TABLE_IN_SMEM = false>
+__device__ __forceinline__ void rotate_il_store(const Packed<T, N>& a, const float2* c, bool ok,
+                                                T* d) {
+  const float qnan = __int_as_float(0x7fc00000);
+  float x[N], y[N];
+  a.get(x);
+#pragma unroll
+  for (int m = 0; m < N / 2; ++m) {
+    const float2 f = ok ? (TABLE_IN_SMEM ? c[m] : __ldg(c + m)) : make_float2(qnan, qnan);
+    const float x0 = x[2 * m], x1 = x[2 * m + 1];
+    if constexpr (!BWD) {
+      y[2 * m] = x0 * f.x - x1 * f.y;
+      y[2 * m + 1] = x1 * f.x + x0 * f.y;
+    } else {
+      y[2 * m] = x0 * f.x + x1 * f.y;
+      y[2 * m + 1] = x1 * f.x - x0 * f.y;
+    }
+  }
+  store_n<T, N>(d, y);
+}
+
+// Everything a RoPE launch needs.  ld* are token strides in elements (a head
+// row h of token t starts at base + t * ld + h * D).
+template <typename T>
+struct RopeArgs {
+  const T* q;
+  const T* k;
+  T* qo;
+  T* ko;
+  const int32_t* pos;
+  const float2* cs;
+  int64_t max_pos, rows;
+  int Hq, Hk, D;
+  int64_t ldq, ldk, ldqo, ldko;
+  __device__ __forceinline__ const T* src(int64_t t, int h) const {
+    return h < Hq ? q + t * ldq + (int64_t)h * D : k + t * ldk + (int64_t)(h - Hq) * D;
+  }
+  __device__ __forceinline__ T* dst(int64_t t, int h) const {
+    return h < Hq ? qo + t * ldqo + (int64_t)h * D : ko + t * ldko + (int64_t)(h - Hq) * D;
+  }
+};
+
+// Register path.  Block of HP * NU threads, NU = units per head row (a unit is
+// the two VEC-element vectors at i and i + D/2 for rotate-half pairing, one
+// VEC-element vector of VEC/2 pairs for interleaved pairing): thread (hl, v)
+// owns unit v of heads hl, hl + HP, ... (HPT of them per pass) of UT
+// consecutive tokens per iteration; token groups are strided by gridDim.  All
+// UT * HPT head loads are issued before the first is used; cos/sin come from
+// L1 / L2 and are reused across the thread's heads.
+template <typename T, int VEC, bool BWD, bool IL, int HPT, int UT>
 __global__ void __launch_bounds__(512)
-rope_kernel(const T* q, const T* k, T* qo, T* ko, const int32_t* __restrict__ pos,
-            const float2* __restrict__ cs, int64_t max_pos, int64_t T_, int Hq, int Hk,
-            int D, int HP) {
-  const int half = D / 2;
-  const int nvh = half / VEC;
-  const int v = threadIdx.x % nvh;
-  const int hl = threadIdx.x / nvh;
-  const int HT = Hq + Hk;
-  const int i0 = v * VEC;
-  for (int64_t tb = (int64_t)blockIdx.x * UT; tb < T_; tb += (int64_t)gridDim.x * UT) {
+rope_kernel(const RopeArgs<T> A, int HP) {
+  const int half = A.D / 2;
+  const int nu = IL ? A.D / VEC : half / VEC;
+  const int v = threadIdx.x % nu;
+  const int hl = threadIdx.x / nu;
+  const int HT = A.Hq + A.Hk;
+  const int i0 = v * VEC;                 // first element of the unit
+  const int c0 = IL ? i0 / 2 : i0;        // first cos/sin entry of the unit
+  for (int64_t tb = (int64_t)blockIdx.x * UT; tb < A.rows; tb += (int64_t)gridDim.x * UT) {
     int p[UT];
 #pragma unroll
-    for (int u = 0; u < UT; ++u) p[u] = tb + u < T_ ? __ldg(pos + tb + u) : 0;
+    for (int u = 0; u < UT; ++u) p[u] = tb + u < A.rows ? __ldg(A.pos + tb + u) : 0;
     for (int h0 = hl; h0 < HT; h0 += HP * HPT) {
       Packed<T, VEC> a[UT][HPT], b[UT][HPT];
 #pragma unroll
@@ -125,26 +169,29 @@ rope_kernel(const T* q, const T* k, T* qo, T* ko, const int32_t* __restrict__ po
 #pragma unroll
         for (int j = 0; j < HPT; ++j) {
           const int h = h0 + j * HP;
-          if (t < T_ && h < HT) {
-            const T* src = h < Hq ? q + ((size_t)t * Hq + h) * D : k + ((size_t)t * Hk + (h - Hq)) * D;
+          if (t < A.rows && h < HT) {
+            const T* src = A.src(t, h);
             a[u][j].load(src + i0);
-            b[u][j].load(src + half + i0);
+            if constexpr (!IL) b[u][j].load(src + half + i0);
           }
         }
       }
 #pragma unroll
       for (int u = 0; u < UT; ++u) {
         const int64_t t = tb + u;
-        if (t >= T_) break;
+        if (t >= A.rows) break;
         // out-of-range position: the table is not read and the outputs are NaN
-        const bool ok = p[u] >= 0 && (int64_t)p[u] < max_pos;
-        const float2* c = cs + (ok ? (size_t)p[u] * half : 0) + i0;
+        const bool ok = p[u] >= 0 && (int64_t)p[u] < A.max_pos;
+        const float2* c = A.cs + (ok ? (size_t)p[u] * half : 0) + c0;
 #pragma unroll
         for (int j = 0; j < HPT; ++j) {
           const int h = h0 + j * HP;
           if (h < HT) {
-            T* dst = h < Hq ? qo + ((size_t)t * Hq + h) * D : ko + ((size_t)t * Hk + (h - Hq)) * D;
-            rotate_store<T, VEC, BWD>(a[u][j], b[u][j], c, ok, dst + i0, dst + half + i0);
+            T* dst = A.dst(t, h);
+            if constexpr (IL)
+              rotate_il_store<T, VEC, BWD>(a[u][j], c, ok, dst + i0);
+            else
+              rotate_store<T, VEC, BWD>(a[u][j], b[u][j], c, ok, dst + i0, dst + half + i0);
           }
         }
       }
@@ -155,12 +202,11 @@ rope_kernel(const T* q, const T* k, T* qo, T* ko, const int32_t* __restrict__ po
 // ---------------------------------------------------------------------------
 // Staged path: a persistent block walks tiles of TT consecutive tokens.  One
 // producer thread reads the tile's positions and fills a stage of a ring of S
-// shared-memory stages with TMA bulk copies: the tile's Q rows and K rows (two
-// contiguous runs) and each token's cos/sin row from the table, all completing
-// on the stage's mbarrier.  S tiles stay in flight per block without holding
-// registers, and the threads then work from shared memory only: rotate and
-// store straight to global memory with 128-bit stores.  Thread (r, v): vector
-// v of the half rows, head lanes r, r + HPL, ...
+// shared-memory stages with TMA bulk copies: the tile's Q rows and K rows and
+// each token's cos/sin row from the table, all completing on the stage's
+// mbarrier.  S tiles stay in flight per block without holding registers, and
+// the threads then work from shared memory only: rotate and store straight to
+// global memory with 128-bit stores.
 // Stage layout: [TT Q rows][TT K rows][TT cos/sin rows][TT positions].
 // ---------------------------------------------------------------------------
 constexpr int kRopeStages = 4;
@@ -188,21 +234,24 @@ __host__ __device__ inline StageGeom stage_geom(int Hq, int Hk, int D, int TT) {
 
 // Warp 0 is the producer (its lane 0 issues); warps 1.. consume.  full[s]
 // completes when stage s holds its tile; empty[s] completes when every
-// consumer warp has finished reading it.  All waits are bounded.
-template <typename T, bool BWD>
+// consumer warp has finished reading it.  All waits are bounded.  With
+// contiguous Q (K) rows a tile's rows are one bulk copy, otherwise one per
+// token.  Consumer thread (r, v): unit v of the head rows, head lanes r,
+// r + HPL, ... (a unit as in the register path).
+template <typename T, bool BWD, bool IL>
 __global__ void __launch_bounds__(kStagedMaxThreads)
-rope_staged_kernel(const T* __restrict__ q, const T* __restrict__ k, T* qo, T* ko,
-                   const int32_t* __restrict__ pos, const float2* __restrict__ cs,
-                   int64_t max_pos, int64_t T_, int Hq, int Hk, int D, int TT, int HPL,
-                   unsigned int* err) {
+rope_staged_kernel(const RopeArgs<T> A, int TT, int HPL, unsigned int* err) {
   constexpr int VEC = VecOf<T>::N;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ uint64_t full[kRopeStages], empty[kRopeStages];
-  const int half = D / 2, nvh = half / VEC, HT = Hq + Hk;
+  const int D = A.D, Hq = A.Hq, Hk = A.Hk;
+  const int half = D / 2, HT = Hq + Hk;
+  const int nu = IL ? D / VEC : half / VEC;
   const int ncw = (int)(blockDim.x / 32) - 1;  // consumer warps
   const StageGeom g = stage_geom<T>(Hq, Hk, D, TT);
-  const int64_t ntiles = (T_ + TT - 1) / TT;
+  const int64_t ntiles = (A.rows + TT - 1) / TT;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const bool qcontig = A.ldq == (int64_t)Hq * D, kcontig = A.ldk == (int64_t)Hk * D;
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < kRopeStages; ++st) {
@@ -226,25 +275,35 @@ rope_staged_kernel(const T* __restrict__ q, const T* __restrict__ k, T* qo, T* k
       }
       fence_proxy_async_smem();
       const int64_t t0 = tile * TT;
-      const int ntok = (int)(T_ - t0 < TT ? T_ - t0 : (int64_t)TT);
+      const int ntok = (int)(A.rows - t0 < TT ? A.rows - t0 : (int64_t)TT);
       unsigned char* base = smem + (size_t)st * g.stage;
       int* spos = reinterpret_cast<int*>(base + g.pos_off());
       uint32_t bytes = (uint32_t)(ntok * (g.qrow + g.krow));
       for (int tok = 0; tok < ntok; ++tok) {
-        const int p = __ldg(pos + t0 + tok);
-        const bool ok = p >= 0 && (int64_t)p < max_pos;
+        const int p = __ldg(A.pos + t0 + tok);
+        const bool ok = p >= 0 && (int64_t)p < A.max_pos;
         spos[tok] = ok ? p : -1;
         if (ok) bytes += (uint32_t)g.csrow;
       }
       mbar_arrive_expect_tx(&full[st], bytes);  // also releases the spos writes
-      bulk_load(base, reinterpret_cast<const unsigned char*>(q) + t0 * g.qrow,
-                (uint32_t)(ntok * g.qrow), &full[st]);
-      if (g.krow)
-        bulk_load(base + (size_t)TT * g.qrow, reinterpret_cast<const unsigned char*>(k) + t0 * g.krow,
-                  (uint32_t)(ntok * g.krow), &full[st]);
+      if (g.qrow) {
+        if (qcontig)
+          bulk_load(base, A.q + t0 * A.ldq, (uint32_t)(ntok * g.qrow), &full[st]);
+        else
+          for (int tok = 0; tok < ntok; ++tok)
+            bulk_load(base + (size_t)tok * g.qrow, A.q + (t0 + tok) * A.ldq, (uint32_t)g.qrow, &full[st]);
+      }
+      if (g.krow) {
+        unsigned char* kb = base + (size_t)TT * g.qrow;
+        if (kcontig)
+          bulk_load(kb, A.k + t0 * A.ldk, (uint32_t)(ntok * g.krow), &full[st]);
+        else
+          for (int tok = 0; tok < ntok; ++tok)
+            bulk_load(kb + (size_t)tok * g.krow, A.k + (t0 + tok) * A.ldk, (uint32_t)g.krow, &full[st]);
+      }
       for (int tok = 0; tok < ntok; ++tok)
         if (spos[tok] >= 0)
-          bulk_load(base + g.cs_off() + (size_t)tok * g.csrow, cs + (size_t)spos[tok] * half,
+          bulk_load(base + g.cs_off() + (size_t)tok * g.csrow, A.cs + (size_t)spos[tok] * half,
                     (uint32_t)g.csrow, &full[st]);
     }
     // Do not leave while copies into this block's shared memory are in flight.
@@ -255,9 +314,10 @@ rope_staged_kernel(const T* __restrict__ q, const T* __restrict__ k, T* qo, T* k
 
   // ---- consumers ----
   const int c = threadIdx.x - 32;
-  const int v = c % nvh, r = c / nvh;
+  const int v = c % nu, r = c / nu;
   const bool active = r < HPL;
   const int i0 = v * VEC;
+  const int c0 = IL ? i0 / 2 : i0;
   int64_t j = 0;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
     const int st = (int)(j % kRopeStages);
@@ -267,7 +327,7 @@ rope_staged_kernel(const T* __restrict__ q, const T* __restrict__ k, T* qo, T* k
     }
     if (active) {
       const int64_t t0 = tile * TT;
-      const int ntok = (int)(T_ - t0 < TT ? T_ - t0 : (int64_t)TT);
+      const int ntok = (int)(A.rows - t0 < TT ? A.rows - t0 : (int64_t)TT);
       const unsigned char* base = smem + (size_t)st * g.stage;
       const unsigned char* sq = base;
       const unsigned char* sk = base + (size_t)TT * g.qrow;
@@ -276,16 +336,21 @@ rope_staged_kernel(const T* __restrict__ q, const T* __restrict__ k, T* qo, T* k
       for (int tok = 0; tok < ntok; ++tok) {
         const int64_t t = t0 + tok;
         const bool ok = spos[tok] >= 0;
-        const float2* cc = scs + (size_t)tok * half + i0;
+        const float2* cc = scs + (size_t)tok * half + c0;
         for (int h = r; h < HT; h += HPL) {
           const T* src = reinterpret_cast<const T*>(h < Hq ? sq + (size_t)tok * g.qrow
                                                            : sk + (size_t)tok * g.krow) +
                          (size_t)(h < Hq ? h : h - Hq) * D;
-          T* dst = h < Hq ? qo + ((size_t)t * Hq + h) * D : ko + ((size_t)t * Hk + (h - Hq)) * D;
-          Packed<T, VEC> a, b;
+          T* dst = A.dst(t, h);
+          Packed<T, VEC> a;
           a.r = ld_shared_v4(src + i0);
-          b.r = ld_shared_v4(src + half + i0);
-          rotate_store<T, VEC, BWD, true>(a, b, cc, ok, dst + i0, dst + half + i0);
+          if constexpr (IL) {
+            rotate_il_store<T, VEC, BWD, true>(a, cc, ok, dst + i0);
+          } else {
+            Packed<T, VEC> b;
+            b.r = ld_shared_v4(src + half + i0);
+            rotate_store<T, VEC, BWD, true>(a, b, cc, ok, dst + i0, dst + half + i0);
+          }
         }
       }
     }
@@ -333,58 +398,44 @@ positions_kernel(const int32_t* __restrict__ cu, int ndoc, int32_t* pos, int64_t
   }
 }
 
-template <typename T, int VEC, bool BWD>
-void rope_launch(int hpt, unsigned grid, int block, int HP, cudaStream_t s, const void* q,
-                 const void* k, void* qo, void* ko, const int32_t* pos, const float* cs,
-                 int64_t max_pos, int64_t rows, int Hq, int Hk, int D) {
-#define GBLN_ROPE(N, U)                                                                   \
-  rope_kernel<T, VEC, BWD, N, U><<<grid, block, 0, s>>>((const T*)q, (const T*)k, (T*)qo,  \
-                                                        (T*)ko, pos, (const float2*)cs,    \
-                                                        max_pos, rows, Hq, Hk, D, HP)
+template <typename T, int VEC, bool BWD, bool IL>
+void rope_launch(int hpt, unsigned grid, int block, int HP, cudaStream_t s, const RopeArgs<T>& A) {
   switch (hpt) {  // heads x tokens per thread and pass
-    case 1: GBLN_ROPE(1, 2); break;
-    case 2: GBLN_ROPE(2, 1); break;
-    default: GBLN_ROPE(4, 1); break;
+    case 1: rope_kernel<T, VEC, BWD, IL, 1, 2><<<grid, block, 0, s>>>(A, HP); break;
+    case 2: rope_kernel<T, VEC, BWD, IL, 2, 1><<<grid, block, 0, s>>>(A, HP); break;
+    default: rope_kernel<T, VEC, BWD, IL, 4, 1><<<grid, block, 0, s>>>(A, HP); break;
   }
-#undef GBLN_ROPE
 }
 
-template <typename T, bool BWD>
-gbln_status rope_typed(const void* q, const void* k, void* qo, void* ko, const int32_t* pos,
-                       const float* cs, int64_t max_pos, int64_t rows, int Hq, int Hk, int D,
-                       cudaStream_t s) {
+template <typename T, bool BWD, bool IL>
+gbln_status rope_typed(const RopeArgs<T>& A, cudaStream_t s) {
   constexpr int VEC = VecOf<T>::N;
-  const int half = D / 2;
-  const bool vec = (half % VEC == 0) && aligned16(q) && aligned16(qo) && aligned16(cs) &&
-                   (Hk == 0 || (aligned16(k) && aligned16(ko)));
+  const int D = A.D, half = D / 2, HT = A.Hq + A.Hk;
+  const bool ld16 = (A.ldq * (int64_t)sizeof(T)) % 16 == 0 && (A.ldqo * (int64_t)sizeof(T)) % 16 == 0 &&
+                    (A.Hk == 0 || ((A.ldk * (int64_t)sizeof(T)) % 16 == 0 &&
+                                   (A.ldko * (int64_t)sizeof(T)) % 16 == 0));
+  const bool vec = (half % VEC == 0) && ld16 && aligned16(A.q) && aligned16(A.qo) &&
+                   aligned16(A.cs) && (A.Hk == 0 || (aligned16(A.k) && aligned16(A.ko)));
   const int sms = sm_count();
   if (sms <= 0) return GBLN_ERR_CUDA;
-  const int nvh = vec ? half / VEC : half;
-  if (nvh > 512) return GBLN_ERR_UNSUPPORTED;  // head size above 1024 (bf16 vector path: 8192)
-  const int HT = Hq + Hk;
-  // Heads per thread: the smallest of 1, 2, 4 that fits the block in 512 threads
-  // (4 with a loop over further heads beyond that).
-  int hpt = 1;
-  while (hpt < 4 && (int64_t)nvh * ((HT + hpt - 1) / hpt) > 512) hpt *= 2;
-  int HP = (HT + hpt - 1) / hpt;
-  if ((int64_t)nvh * HP > 512) HP = 512 / nvh;
-  const int block = nvh * HP;
-  const int per_sm = block > 0 ? 2048 / block : 1;
-  const int ut = hpt == 1 ? 2 : 1;
-  const unsigned grid = grid_for((rows + ut - 1) / ut, 1, (int64_t)sms * (per_sm > 0 ? per_sm : 1));
+  // elements per unit: VEC on the vector path; on the element-wise path 1
+  // (rotate-half) or one pair (interleaved)
+  const int unit = vec ? VEC : (IL ? 2 : 1);
+  const int nu = IL ? D / unit : half / unit;
+  if (nu > 512) return GBLN_ERR_UNSUPPORTED;  // head size above 1024 (bf16 vector path: 8192)
   // Staged (TMA bulk) path: vector layout and a token small enough that four
   // stages of at least one token fit two blocks per SM.  In place is fine: a
   // tile is completely in shared memory before any of its outputs is stored.
   const size_t tok_bytes = (size_t)HT * D * sizeof(T) + (size_t)half * sizeof(float2);
-  if (vec && nvh <= 256 && tok_bytes <= kStageTarget) {
+  if (vec && nu <= 256 && tok_bytes <= kStageTarget) {
     unsigned int* err = device_error_word();
     if (!err) return GBLN_ERR_CUDA;
     const int TT = (int)(kStageTarget / tok_bytes);
-    const StageGeom geo = stage_geom<T>(Hq, Hk, D, TT);
+    const StageGeom geo = stage_geom<T>(A.Hq, A.Hk, D, TT);
     const size_t smem = (size_t)kRopeStages * geo.stage;
-    const int hpl = 256 / nvh < HT ? 256 / nvh : HT;
-    const int threads = 32 + ((nvh * hpl + 31) / 32) * 32;
-    auto kern = rope_staged_kernel<T, BWD>;
+    const int hpl = 256 / nu < HT ? 256 / nu : HT;
+    const int threads = 32 + ((nu * hpl + 31) / 32) * 32;
+    auto kern = rope_staged_kernel<T, BWD, IL>;
     static std::atomic<uint64_t> attr_done{0};  // one bit per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return GBLN_ERR_CUDA; }
@@ -397,35 +448,61 @@ gbln_status rope_typed(const void* q, const void* k, void* qo, void* ko, const i
       }
       attr_done.fetch_or(bit, std::memory_order_acq_rel);
     }
-    const int64_t ntiles = (rows + TT - 1) / TT;
+    const int64_t ntiles = (A.rows + TT - 1) / TT;
     const unsigned sgrid = grid_for(ntiles, 1, (int64_t)sms * 2);
-    kern<<<sgrid, threads, smem, s>>>((const T*)q, (const T*)k, (T*)qo, (T*)ko, pos,
-                                      (const float2*)cs, max_pos, rows, Hq, Hk, D, TT, hpl, err);
+    kern<<<sgrid, threads, smem, s>>>(A, TT, hpl, err);
     return launch_status();
   }
+  // Heads per thread: the smallest of 1, 2, 4 that fits the block in 512 threads
+  // (4 with a loop over further heads beyond that).
+  int hpt = 1;
+  while (hpt < 4 && (int64_t)nu * ((HT + hpt - 1) / hpt) > 512) hpt *= 2;
+  int HP = (HT + hpt - 1) / hpt;
+  if ((int64_t)nu * HP > 512) HP = 512 / nu;
+  const int block = nu * HP;
+  const int per_sm = block > 0 ? 2048 / block : 1;
+  const int ut = hpt == 1 ? 2 : 1;
+  const unsigned grid = grid_for((A.rows + ut - 1) / ut, 1, (int64_t)sms * (per_sm > 0 ? per_sm : 1));
   if (vec)
-    rope_launch<T, VEC, BWD>(hpt, grid, block, HP, s, q, k, qo, ko, pos, cs, max_pos, rows, Hq, Hk, D);
+    rope_launch<T, VEC, BWD, IL>(hpt, grid, block, HP, s, A);
+  else if (IL)
+    rope_launch<T, 2, BWD, IL>(hpt, grid, block, HP, s, A);
   else
-    rope_launch<T, 1, BWD>(hpt, grid, block, HP, s, q, k, qo, ko, pos, cs, max_pos, rows, Hq, Hk, D);
+    rope_launch<T, 1, BWD, IL>(hpt, grid, block, HP, s, A);
   return launch_status();
 }
 
 template <bool BWD>
 gbln_status rope_entry(const void* q, const void* k, void* qo, void* ko, const int32_t* pos,
                        const float* cs, int64_t max_pos, int64_t T, int32_t Hq, int32_t Hk,
-                       int32_t D, gbln_dtype io, gbln_stream_t stream) {
-  if (!dtype_ok(io)) return GBLN_ERR_INVALID_ARG;
-  if (T < 0 || Hq < 0 || Hk < 0 || Hq + Hk <= 0 || D <= 0 || (D & 1) || max_pos < 0)
+                       int32_t D, int64_t ldq, int64_t ldk, int64_t ldqo, int64_t ldko,
+                       int pairing, gbln_dtype io, gbln_stream_t stream) {
+  if (!dtype_ok(io) || (pairing != GBLN_ROPE_HALF && pairing != GBLN_ROPE_INTERLEAVED))
+    return GBLN_ERR_INVALID_ARG;
+  if (T < 0 || T > (1LL << 40) || Hq < 0 || Hk < 0 || Hq + Hk <= 0 || D <= 0 || (D & 1) ||
+      max_pos < 0)
     return GBLN_ERR_INVALID_ARG;
   if ((int64_t)(Hq + Hk) * D > (1 << 24)) return GBLN_ERR_INVALID_ARG;
+  const int64_t qw = (int64_t)Hq * D, kw = (int64_t)Hk * D, lim = 1LL << 40;
+  if (ldq < qw || ldqo < qw || (Hk > 0 && (ldk < kw || ldko < kw))) return GBLN_ERR_INVALID_ARG;
+  if (ldq > lim || ldqo > lim || ldk > lim || ldko > lim) return GBLN_ERR_INVALID_ARG;
   if (T == 0) return GBLN_OK;  // nothing is read or written: pointers are not examined
   if (!pos || !cs) return GBLN_ERR_INVALID_ARG;
   if (Hq > 0 && (!q || !qo)) return GBLN_ERR_INVALID_ARG;
   if (Hk > 0 && (!k || !ko)) return GBLN_ERR_INVALID_ARG;
   if (((uintptr_t)cs & 7u) != 0) return GBLN_ERR_INVALID_ARG;  // float2 table
   cudaStream_t s = (cudaStream_t)stream;
-  if (io == GBLN_F32) return rope_typed<float, BWD>(q, k, qo, ko, pos, cs, max_pos, T, Hq, Hk, D, s);
-  return rope_typed<bf16, BWD>(q, k, qo, ko, pos, cs, max_pos, T, Hq, Hk, D, s);
+  const bool il = pairing == GBLN_ROPE_INTERLEAVED;
+#define GBLN_ROPE_ARGS(TY)                                                                     \
+  RopeArgs<TY> A{(const TY*)q, (const TY*)k, (TY*)qo, (TY*)ko, pos, (const float2*)cs, max_pos, \
+                 T, Hq, Hk, D, ldq, Hk > 0 ? ldk : 0, ldqo, Hk > 0 ? ldko : 0}
+  if (io == GBLN_F32) {
+    GBLN_ROPE_ARGS(float);
+    return il ? rope_typed<float, BWD, true>(A, s) : rope_typed<float, BWD, false>(A, s);
+  }
+  GBLN_ROPE_ARGS(bf16);
+  return il ? rope_typed<bf16, BWD, true>(A, s) : rope_typed<bf16, BWD, false>(A, s);
+#undef GBLN_ROPE_ARGS
 }
 
 }  // namespace
@@ -451,16 +528,38 @@ extern "C" gbln_status gbln_rope_fwd(const void* q, const void* k, void* q_out, 
                                      const int32_t* positions, const float* cos_sin,
                                      int64_t max_pos, int64_t T, int32_t Hq, int32_t Hk,
                                      int32_t D, gbln_dtype io, gbln_stream_t stream) {
-  return rope_entry<false>(q, k, q_out, k_out, positions, cos_sin, max_pos, T, Hq, Hk, D, io,
-                           stream);
+  const int64_t qw = (int64_t)Hq * D, kw = (int64_t)Hk * D;
+  return rope_entry<false>(q, k, q_out, k_out, positions, cos_sin, max_pos, T, Hq, Hk, D, qw, kw,
+                           qw, kw, GBLN_ROPE_HALF, io, stream);
 }
 
 extern "C" gbln_status gbln_rope_bwd(const void* dq, const void* dk, void* dq_in, void* dk_in,
                                      const int32_t* positions, const float* cos_sin,
                                      int64_t max_pos, int64_t T, int32_t Hq, int32_t Hk,
                                      int32_t D, gbln_dtype io, gbln_stream_t stream) {
-  return rope_entry<true>(dq, dk, dq_in, dk_in, positions, cos_sin, max_pos, T, Hq, Hk, D, io,
-                          stream);
+  const int64_t qw = (int64_t)Hq * D, kw = (int64_t)Hk * D;
+  return rope_entry<true>(dq, dk, dq_in, dk_in, positions, cos_sin, max_pos, T, Hq, Hk, D, qw, kw,
+                          qw, kw, GBLN_ROPE_HALF, io, stream);
+}
+
+extern "C" gbln_status gbln_rope_fwd_ex(const void* q, const void* k, void* q_out, void* k_out,
+                                        const int32_t* positions, const float* cos_sin,
+                                        int64_t max_pos, int64_t T, int32_t Hq, int32_t Hk,
+                                        int32_t D, int64_t ld_q, int64_t ld_k, int64_t ld_q_out,
+                                        int64_t ld_k_out, gbln_rope_pairing pairing,
+                                        gbln_dtype io, gbln_stream_t stream) {
+  return rope_entry<false>(q, k, q_out, k_out, positions, cos_sin, max_pos, T, Hq, Hk, D, ld_q,
+                           ld_k, ld_q_out, ld_k_out, pairing, io, stream);
+}
+
+extern "C" gbln_status gbln_rope_bwd_ex(const void* dq, const void* dk, void* dq_in, void* dk_in,
+                                        const int32_t* positions, const float* cos_sin,
+                                        int64_t max_pos, int64_t T, int32_t Hq, int32_t Hk,
+                                        int32_t D, int64_t ld_dq, int64_t ld_dk, int64_t ld_dq_in,
+                                        int64_t ld_dk_in, gbln_rope_pairing pairing,
+                                        gbln_dtype io, gbln_stream_t stream) {
+  return rope_entry<true>(dq, dk, dq_in, dk_in, positions, cos_sin, max_pos, T, Hq, Hk, D, ld_dq,
+                          ld_dk, ld_dq_in, ld_dk_in, pairing, io, stream);
 }
 
 extern "C" gbln_status gbln_positions_from_cu_seqlens(const int32_t* cu_seqlens, int32_t ndoc,

@@ -112,6 +112,20 @@ def test_rope_rejects(lib):
     assert lib.gbln_rope_table(FAKE, 0, 8, 1e4, None) == OK
 
 
+def test_rope_ex_rejects(lib):
+    def ex(fn, ldq=64, ldk=16, ldqo=64, ldko=16, pairing=0, T=4, q=FAKE):
+        return getattr(lib, fn)(q, FAKE, FAKE, FAKE, FAKE, FAKE, 100, T, 4, 1, 16, ldq, ldk, ldqo, ldko,
+                                pairing, BF16, None)
+    for fn in ("gbln_rope_fwd_ex", "gbln_rope_bwd_ex"):
+        assert ex(fn, ldq=63) == INVALID
+        assert ex(fn, ldk=15) == INVALID
+        assert ex(fn, ldqo=10) == INVALID
+        assert ex(fn, ldko=0) == INVALID
+        assert ex(fn, pairing=2) == INVALID
+        assert ex(fn, q=None) == INVALID
+        assert ex(fn, T=0, q=None) == OK
+
+
 def test_positions_rejects(lib):
     f = lib.gbln_positions_from_cu_seqlens
     assert f(FAKE, 2, None, 10, None) == INVALID
@@ -137,6 +151,24 @@ def test_swiglu_rejects(lib):
         args[i] = None
         assert lib.gbln_swiglu_bwd(*args, 4, 8, BF16, None) == INVALID
     assert lib.gbln_swiglu_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 8, F32, None) == OK
+
+
+def test_glu_and_act_reject(lib):
+    f = FAKE
+    assert lib.gbln_glu_fwd(f, f, f, 4, 8, 7, 8, 8, 0, BF16, None) == INVALID  # ld < I
+    assert lib.gbln_glu_fwd(f, f, f, 4, 8, 8, 8, 8, 9, BF16, None) == INVALID  # bad act
+    assert lib.gbln_glu_fwd(None, f, f, 4, 8, 8, 8, 8, 0, BF16, None) == INVALID
+    assert lib.gbln_glu_fwd(f, f, f, 4, 0, 8, 8, 8, 0, BF16, None) == INVALID
+    assert lib.gbln_glu_fwd(None, None, None, 0, 8, 8, 8, 8, 0, BF16, None) == OK
+    assert lib.gbln_glu_bwd(f, f, f, f, f, 4, 8, 8, 8, 8, 8, 3, 0, BF16, None) == INVALID
+    assert lib.gbln_glu_bwd(f, f, f, None, f, 4, 8, 8, 8, 8, 8, 8, 0, BF16, None) == INVALID
+    assert lib.gbln_glu_bwd(None, None, None, None, None, 0, 8, 8, 8, 8, 8, 8, 3, F32, None) == OK
+    assert lib.gbln_act_fwd(None, f, 4, 0, BF16, None) == INVALID
+    assert lib.gbln_act_fwd(f, f, 4, 4, BF16, None) == INVALID
+    assert lib.gbln_act_fwd(f, f, -1, 0, BF16, None) == INVALID
+    assert lib.gbln_act_fwd(None, None, 0, 2, F32, None) == OK
+    assert lib.gbln_act_bwd(f, None, f, 4, 0, BF16, None) == INVALID
+    assert lib.gbln_act_bwd(None, None, None, 0, 1, BF16, None) == OK
 
 
 def test_device_error_rejects_null(lib):

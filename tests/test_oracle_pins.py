@@ -342,3 +342,88 @@ def test_positions_brute_force():
     for start in cu[:-1]:
         assert pos[start] == 0
     assert oracle.positions_from_doc_lengths([]).size == 0
+
+
+# ---------------------------------------------------------------------------
+# Gated / plain activations
+# ---------------------------------------------------------------------------
+
+def test_gelu_hand_values():
+    for row in open(os.path.join(GOLDEN, "gelu.txt"), encoding="utf-8"):
+        row = row.strip()
+        if not row or row.startswith("#"):
+            continue
+        form, x, val, tol = row.split()
+        name = "gelu_erf" if form == "erf" else "gelu_tanh"
+        got = oracle.act(name, np.array([float(x)]))[0]
+        assert got == pytest.approx(float(val), abs=float(tol) + 1e-300), (name, x, got)
+
+
+def test_activation_identities():
+    x = np.linspace(-6, 6, 241)
+    # GeLU(x) - GeLU(-x) = x in both forms (Phi(x) + Phi(-x) = 1; tanh is odd)
+    for name in ("gelu_erf", "gelu_tanh"):
+        assert np.allclose(oracle.act(name, x) - oracle.act(name, -x), x, atol=1e-13)
+    # the two GeLU forms agree to the known approximation error (< 1e-3 on this range)
+    assert np.max(np.abs(oracle.act("gelu_erf", x) - oracle.act("gelu_tanh", x))) < 1e-3
+    assert np.array_equal(oracle.act("relu", x), np.where(x > 0, x, 0.0))
+    assert np.allclose(oracle.act("silu", x), x / (1 + np.exp(-x)), rtol=1e-14)
+    # SwiGLU is the SiLU-gated unit
+    u = np.cos(x)
+    assert np.array_equal(oracle.glu_fwd("silu", x, u), oracle.swiglu_fwd(x, u))
+    dg, du = oracle.glu_bwd("silu", np.sin(x), x, u)
+    dg2, du2 = oracle.swiglu_bwd(np.sin(x), x, u)
+    assert np.allclose(dg, dg2, rtol=1e-13, atol=1e-15) and np.allclose(du, du2, rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("name", ["silu", "gelu_tanh", "gelu_erf", "relu"])
+def test_activation_grad_central_differences(name):
+    x = np.array([-4.1, -2.3, -0.7, -0.05, 0.13, 0.9, 1.7, 3.2, 5.5])
+    d = 1e-6
+    fd = (oracle.act(name, x + d) - oracle.act(name, x - d)) / (2 * d)
+    assert np.allclose(oracle.act_grad(name, x), fd, rtol=1e-7, atol=1e-9)
+    g = np.array([0.4, -1.2, 2.5])
+    u = np.array([1.5, -0.3, 0.8])
+    dout = np.array([0.7, 2.0, -1.1])
+    dgate, dup = oracle.glu_bwd(name, dout, g, u)
+    for i in range(3):
+        gp = g.copy(); gp[i] += d
+        gm = g.copy(); gm[i] -= d
+        fd = (np.sum(dout * oracle.glu_fwd(name, gp, u)) - np.sum(dout * oracle.glu_fwd(name, gm, u))) / (2 * d)
+        assert dgate[i] == pytest.approx(fd, rel=1e-7, abs=1e-9)
+        up_ = u.copy(); up_[i] += d
+        um = u.copy(); um[i] -= d
+        fd = (np.sum(dout * oracle.glu_fwd(name, g, up_)) - np.sum(dout * oracle.glu_fwd(name, g, um))) / (2 * d)
+        assert dup[i] == pytest.approx(fd, rel=1e-7, abs=1e-9)
+
+
+def test_rope_interleaved_is_a_permuted_rotate_half():
+    # Interleaved pairing (2i, 2i+1) = rotate-half pairing after de-interleaving
+    # the head (evens then odds) and re-interleaving the result.
+    rng = np.random.default_rng(20)
+    T, Hh, D = 4, 3, 16
+    x = rng.normal(size=(T, Hh, D))
+    pos = np.array([0, 7, 300, 9000])
+    perm = np.concatenate([np.arange(0, D, 2), np.arange(1, D, 2)])
+    inv = np.argsort(perm)
+    via_half = oracle.rope_fwd(x[..., perm], pos, 1e4)[..., inv]
+    assert np.allclose(oracle.rope_fwd(x, pos, 1e4, "interleaved"), via_half, rtol=1e-14, atol=1e-14)
+    y = oracle.rope_fwd(x, pos, 1e4, "interleaved")
+    assert np.allclose(oracle.rope_bwd(y, pos, 1e4, "interleaved"), x, atol=1e-12)
+
+
+def test_rope_interleaved_equals_complex_multiplication():
+    rng = np.random.default_rng(21)
+    D, theta = 8, 500000.0
+    x = rng.normal(size=(2, 1, D))
+    pos = np.array([3, 12345])
+    got = oracle.rope_fwd(x, pos, theta, "interleaved")
+    for t in range(2):
+        for i in range(D // 2):
+            z = complex(x[t, 0, 2 * i], x[t, 0, 2 * i + 1]) * cmath.exp(1j * pos[t] * theta ** (-2.0 * i / D))
+            assert got[t, 0, 2 * i] == pytest.approx(z.real, abs=1e-11)
+            assert got[t, 0, 2 * i + 1] == pytest.approx(z.imag, abs=1e-11)
+    # with two elements both pairings are the same rotation
+    x2 = rng.normal(size=(3, 2, 2))
+    p2 = np.array([1, 5, 9])
+    assert np.array_equal(oracle.rope_fwd(x2, p2, 1e4, "interleaved"), oracle.rope_fwd(x2, p2, 1e4))
