@@ -391,6 +391,93 @@ def run_single_op(args, wl, device):
                       "frac": round(gbs / peak, 4), "peak": peak, "peak_kind": f"of {peak_kind}"}))
 
 
+def run_next_ops(args, wl, device):
+    """Time the operators beyond the step (gated units with other activations and
+    packed layouts, plain activations, strided / interleaved RoPE, LayerNorm) at
+    the workload's widths: K launches each, CUDA events around each launch, L2
+    flushed in between.  One JSON line with per-operator time and GB/s."""
+    import rmsnorm_fwd_bwd_03_gb300 as gb
+    from rmsnorm_fwd_bwd_03_gb300._build import build_library
+    from rmsnorm_fwd_bwd_03_gb300.workload import scaled
+    build_library()
+    lib = gb.library()
+    if args.tokens:
+        wl = scaled(wl, args.tokens, f"_T{args.tokens}")
+    T, H, I, D, Hq, Hk = wl.T, wl.H, wl.I, wl.D, wl.Hq, wl.Hk
+    dt = wl.dtype
+    b = 2 if dt == torch.bfloat16 else 4
+    io = gb.BF16 if dt == torch.bfloat16 else gb.F32
+    s = torch.cuda.current_stream(device).cuda_stream
+    g = torch.Generator(device=device)
+    g.manual_seed(0)
+    rnd = lambda *shape: torch.randn(shape, generator=g, device=device).to(dt)  # noqa: E731
+    p = lambda t: t.data_ptr()  # noqa: E731
+    ops = {}
+
+    # gated units on a packed [T, 2I] gate|up tensor and a packed [T, 2I] gradient
+    packed, dout = rnd(T, 2 * I), rnd(T, I)
+    out, grad = torch.empty(T, I, dtype=dt, device=device), torch.empty(T, 2 * I, dtype=dt, device=device)
+    for act in ("silu", "gelu_tanh", "gelu_erf", "relu"):
+        a = gb.ACT[act]
+        ops[f"glu_fwd_packed_{act}"] = (lib.gbln_glu_fwd, (p(packed), p(packed) + I * b, p(out), T, I, 2 * I, 2 * I, I, a, io, s), 3 * T * I * b)
+        ops[f"glu_bwd_packed_{act}"] = (lib.gbln_glu_bwd, (p(dout), p(packed), p(packed) + I * b, p(grad), p(grad) + I * b, T, I, I, 2 * I, 2 * I, 2 * I, 2 * I, a, io, s), 5 * T * I * b)
+    x, dy = rnd(T, I), rnd(T, I)
+    y = torch.empty_like(x)
+    ops["act_fwd_gelu_tanh"] = (lib.gbln_act_fwd, (p(x), p(y), T * I, gb.ACT["gelu_tanh"], io, s), 2 * T * I * b)
+    ops["act_bwd_gelu_tanh"] = (lib.gbln_act_bwd, (p(dy), p(x), p(y), T * I, gb.ACT["gelu_tanh"], io, s), 3 * T * I * b)
+
+    # RoPE: Q and K rotated in place inside one packed QKV tensor; interleaved pairing
+    W = (Hq + 2 * Hk) * D
+    qkv = rnd(T, W)
+    pos = gb.positions_from_cu_seqlens(torch.as_tensor(wl.cu_seqlens(), dtype=torch.int32, device=device), T)
+    table = gb.rope_table(wl.max_pos(), D, wl.theta, device=device)
+    rope_bytes = 2 * T * (Hq + Hk) * D * b + 4 * T
+    ops["rope_fwd_packed_qkv_in_place"] = (lib.gbln_rope_fwd_ex, (p(qkv), p(qkv) + Hq * D * b, p(qkv), p(qkv) + Hq * D * b, p(pos), p(table), table.shape[0], T, Hq, Hk, D, W, W, W, W, 0, io, s), rope_bytes)
+    q, k = rnd(T, Hq, D), rnd(T, Hk, D)
+    qo, ko = torch.empty_like(q), torch.empty_like(k)
+    ops["rope_fwd_interleaved"] = (lib.gbln_rope_fwd_ex, (p(q), p(k), p(qo), p(ko), p(pos), p(table), table.shape[0], T, Hq, Hk, D, Hq * D, Hk * D, Hq * D, Hk * D, 1, io, s), rope_bytes)
+
+    # LayerNorm with residual and bias
+    xl, rl, dyl, drl = rnd(T, H), rnd(T, H), rnd(T, H), rnd(T, H)
+    wgt, bias = (1 + 0.1 * torch.randn(H, generator=g, device=device)).to(dt), rnd(H)
+    yl, hl = torch.empty_like(xl), torch.empty_like(xl)
+    mean, rstd = torch.empty(T, device=device), torch.empty(T, device=device)
+    dxl = torch.empty_like(xl)
+    P = gb.layernorm_bwd_num_partials(T, H, dt)
+    part = torch.empty(P, 2 * H, device=device)
+    dwl, dbl = torch.empty(H, device=device), torch.empty(H, device=device)
+    ops["layernorm_fwd"] = (lib.gbln_layernorm_fwd, (p(xl), p(rl), p(wgt), p(bias), p(yl), p(hl), p(mean), p(rstd), T, H, wl.eps, io, io, s), 4 * T * H * b + 8 * T + 2 * H * b)
+    ops["layernorm_bwd"] = (lib.gbln_layernorm_bwd, (p(dyl), p(drl), p(hl), p(wgt), p(mean), p(rstd), p(dxl), p(part), P, T, H, io, io, s), 4 * T * H * b + 8 * T + H * b)
+    ops["layernorm_dwdb_finalize"] = (lib.gbln_layernorm_dwdb_finalize, (p(part), P, H, p(dwl), p(dbl), 0, s), 0)
+
+    flush = L2Flush(device)
+    peak, peak_kind = _measured_peak()
+    res = {}
+    for name in ["layernorm_fwd", "layernorm_bwd", "layernorm_dwdb_finalize"] + [n for n in ops if not n.startswith("layernorm")]:
+        fn, fargs, alg = ops[name]
+        for _ in range(args.warmup):
+            flush()
+            st = fn(*fargs)
+            if st != 0:
+                raise RuntimeError(f"{name}: status {st}")
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(args.steps):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn(*fargs)
+            e1.record()
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(c) for a, c in evs) / args.steps
+        gbs = alg / (ms * 1e-3) / 1e9 if alg else 0.0
+        res[name] = {"ms": round(ms, 5), "alg_bytes": alg, "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    err = gb.device_error()
+    print(json.dumps({"next_ops": res, "workload": wl.name, "tokens": T, "launches_each": args.steps,
+                      "peak": peak, "peak_kind": f"of {peak_kind}", "device_error_word": err}))
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -428,7 +515,10 @@ def main():
     ap.add_argument("--op", choices=OPS, default=None,
                     help="time one operator alone (also the driver for ncu captures)")
     ap.add_argument("--tokens", type=int, default=0,
-                    help="with --op: use the workload's widths with this many tokens")
+                    help="with --op / --next: use the workload's widths with this many tokens")
+    ap.add_argument("--next", action="store_true",
+                    help="time the operators beyond the step (other activations, packed layouts, "
+                         "strided / interleaved RoPE, LayerNorm) at the workload's widths")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -479,6 +569,8 @@ def main():
 
     if args.op:
         return run_single_op(args, wl, device)
+    if args.next:
+        return run_next_ops(args, wl, device)
 
     step = Step(wl, device, seed=rank)
     stream = torch.cuda.current_stream(device)

@@ -187,6 +187,45 @@ gbln_status gbln_rmsnorm_bwd_noalloc(const void* dy, const void* dresidual_out, 
                                      gbln_dtype io, gbln_dtype wt, gbln_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* LayerNorm with fused residual add ([FL] Transformer Block 结构:             */
+/* normalization LayerNorm / RMSNorm)                                         */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Forward, per row t of H channels:
+ *   h = x + residual (rounded to io; h = x when residual is NULL)
+ *   mean[t] = mean_j h;  var = mean_j (h - mean)^2;  rstd[t] = 1 / sqrt(var + eps)
+ *   y = weight * (h - mean) * rstd + bias  (bias NULL = no bias; one rounding to io)
+ * Arguments as gbln_rmsnorm_fwd, plus bias [H] wt (nullable) and mean [T] float32
+ * (written; the backward pass reads it with rstd).
+ */
+gbln_status gbln_layernorm_fwd(const void* x, const void* residual, const void* weight,
+                               const void* bias, void* y, void* residual_out, float* mean,
+                               float* rstd, int64_t T, int64_t H, float eps, gbln_dtype io,
+                               gbln_dtype wt, gbln_stream_t stream);
+
+/* Rows P of the [P, 2H] float32 dW|dB workspace of gbln_layernorm_bwd (as gbln_rmsnorm_bwd_num_partials). */
+int64_t gbln_layernorm_bwd_num_partials(int64_t T, int64_t H, gbln_dtype io);
+
+/*
+ * Backward, first pass.  With n = (h - mean) * rstd and g = dy * weight, per row:
+ *   dx = rstd * (g - mean_j g - n * mean_j(g * n)) + dresidual_out
+ *   partial[p, 0:H]  = sum over the rows of block p of dy * n   (dW)
+ *   partial[p, H:2H] = sum over the rows of block p of dy       (dB)
+ * Arguments as gbln_rmsnorm_bwd, plus mean [T] from the forward; the workspace is
+ * [P_cap, 2H] float32.  Bitwise reproducible for a fixed shape and GPU model.
+ */
+gbln_status gbln_layernorm_bwd(const void* dy, const void* dresidual_out, const void* h,
+                               const void* weight, const float* mean, const float* rstd,
+                               void* dx, float* dwdb_partial, int64_t P_cap, int64_t T, int64_t H,
+                               gbln_dtype io, gbln_dtype wt, gbln_stream_t stream);
+
+/* Second pass: dw[j] (+)= sum_p partial[p, j], db[j] (+)= sum_p partial[p, H + j], fixed order. */
+gbln_status gbln_layernorm_dwdb_finalize(const float* dwdb_partial, int64_t P, int64_t H,
+                                         float* dw, float* db, int accumulate,
+                                         gbln_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* Rotary position embedding on Q and K ([FL] attention with RoPE, rotary     */
 /* type default with theta; [LF] fused RoPE; [HF] §Liger)                     */
 /* ------------------------------------------------------------------------- */

@@ -49,6 +49,8 @@ __all__ = [
     "rmsnorm_fwd",
     "rmsnorm_bwd",
     "rmsnorm_dw",
+    "layernorm_fwd",
+    "layernorm_bwd",
     "rope_inv_freq",
     "rope_fwd",
     "rope_bwd",
@@ -165,6 +167,53 @@ def rmsnorm_dw(dy, h, eps, rows_per_chunk=4096):
         rstd = 1.0 / np.sqrt(np.mean(hb * hb, axis=-1) + eps)
         dw += np.sum(dyb * hb * rstd[:, None], axis=0)
     return dw
+
+
+# ---------------------------------------------------------------------------
+# LayerNorm with fused residual add ("Fast-LLM: 高效大语言模型训练框架", §三 Transformer
+# Block 结构: normalization LayerNorm / RMSNorm).  Standard form: subtract the
+# row mean, divide by sqrt(variance + eps) (biased variance), scale by the
+# weight, add the bias.
+# ---------------------------------------------------------------------------
+
+def layernorm_fwd(x, residual, weight, bias, eps, io=None):
+    """Returns ``(y, h, mean, rstd)``:
+      h    = round_io(x + residual)            (x if no residual)
+      mean = mean(h);  var = mean((h - mean)**2);  rstd = 1 / sqrt(var + eps)
+      y    = weight * (h - mean) * rstd + bias  (bias None = 0), exact
+    """
+    x = np.asarray(x, dtype=np.float64)
+    if residual is None:
+        h = x
+    else:
+        h = round_io(x + np.asarray(residual, dtype=np.float64), io)
+    mean = np.mean(h, axis=-1)
+    c = h - mean[..., None]
+    var = np.mean(c * c, axis=-1)
+    rstd = 1.0 / np.sqrt(var + eps)
+    y = np.asarray(weight, dtype=np.float64) * c * rstd[..., None]
+    if bias is not None:
+        y = y + np.asarray(bias, dtype=np.float64)
+    return y, h, mean, rstd
+
+
+def layernorm_bwd(dy, dres, h, weight, eps):
+    """Gradients of :func:`layernorm_fwd`.  With n = (h - mean) * rstd, g = dy * weight:
+      dh = rstd * (g - mean(g) - n * mean(g * n));  dx = dh + dres
+      dW = sum over rows of dy * n;  dB = sum over rows of dy
+    Returns ``(dx, dW, dB)``.
+    """
+    dy = np.asarray(dy, dtype=np.float64)
+    h = np.asarray(h, dtype=np.float64)
+    mean = np.mean(h, axis=-1)
+    c = h - mean[..., None]
+    rstd = 1.0 / np.sqrt(np.mean(c * c, axis=-1) + eps)
+    n = c * rstd[..., None]
+    g = dy * np.asarray(weight, dtype=np.float64)
+    dx = rstd[..., None] * (g - np.mean(g, axis=-1)[..., None] - n * np.mean(g * n, axis=-1)[..., None])
+    if dres is not None:
+        dx = dx + np.asarray(dres, dtype=np.float64)
+    return dx, np.sum(dy * n, axis=0), np.sum(dy, axis=0)
 
 
 # ---------------------------------------------------------------------------

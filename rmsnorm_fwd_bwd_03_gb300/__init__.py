@@ -20,7 +20,8 @@ from ._build import LIB as _LIB_PATH
 __all__ = [
     "GblnError", "library", "library_path", "status_string", "version", "device_error",
     "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_num_partials", "rmsnorm_dw_finalize",
-    "rmsnorm_bwd_noalloc",
+    "rmsnorm_bwd_noalloc", "layernorm_fwd", "layernorm_bwd", "layernorm_bwd_num_partials",
+    "layernorm_dwdb_finalize",
     "rope_table", "rope_fwd", "rope_bwd", "rope_fwd_ex", "rope_bwd_ex", "positions_from_cu_seqlens",
     "swiglu_fwd", "swiglu_bwd", "glu_fwd", "glu_bwd", "act_fwd", "act_bwd", "ACT",
     "F32", "BF16",
@@ -47,6 +48,10 @@ _SIGNATURES = {
     "gbln_rmsnorm_bwd_num_partials": (_i64, [_i64, _i64, ctypes.c_int]),
     "gbln_rmsnorm_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
     "gbln_rmsnorm_dw_finalize": (ctypes.c_int, [_vp, _i64, _i64, _vp, ctypes.c_int, _vp]),
+    "gbln_layernorm_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, ctypes.c_int, ctypes.c_int, _vp]),
+    "gbln_layernorm_bwd_num_partials": (_i64, [_i64, _i64, ctypes.c_int]),
+    "gbln_layernorm_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
+    "gbln_layernorm_dwdb_finalize": (ctypes.c_int, [_vp, _i64, _i64, _vp, _vp, ctypes.c_int, _vp]),
     "gbln_rmsnorm_bwd_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
     "gbln_rope_table": (ctypes.c_int, [_vp, _i64, _i32, _f64, _vp]),
     "gbln_rope_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, ctypes.c_int, _vp]),
@@ -218,6 +223,71 @@ def rmsnorm_bwd_noalloc(dy, h, weight, rstd, dresidual_out=None, *, dx=None, dw=
         _opt(rstd, "rstd"), _opt(dx, "dx"), _dev(dw, "dw"), T, H, _io(dy), _io(weight), _stream(dw))
     _check("gbln_rmsnorm_bwd_noalloc", st)
     return dx, dw
+
+
+# ---------------------------------------------------------------------------
+# LayerNorm
+# ---------------------------------------------------------------------------
+
+def layernorm_fwd(x, weight, eps, residual=None, bias=None, *, y=None, residual_out=None, mean=None,
+                  rstd=None):
+    """``gbln_layernorm_fwd``.  Returns ``(y, h, mean, rstd)`` (mean, rstd float32 [T])."""
+    H = x.shape[-1]
+    T = x.numel() // H if H else 0
+    if y is None:
+        y = torch.empty_like(x)
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(x)
+    if mean is None:
+        mean = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    if rstd is None:
+        rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    st = library().gbln_layernorm_fwd(
+        _dev(x, "x"), _opt(residual, "residual"), _dev(weight, "weight"), _opt(bias, "bias"),
+        _dev(y, "y"), _opt(residual_out, "residual_out") if residual is not None else None,
+        _dev(mean, "mean"), _dev(rstd, "rstd"), T, H, float(eps), _io(x), _io(weight), _stream(x))
+    _check("gbln_layernorm_fwd", st)
+    return y, (residual_out if residual is not None else x), mean, rstd
+
+
+def layernorm_bwd_num_partials(T: int, H: int, dtype=torch.bfloat16) -> int:
+    """``gbln_layernorm_bwd_num_partials``: rows P of the [P, 2H] float32 dW|dB workspace."""
+    P = library().gbln_layernorm_bwd_num_partials(int(T), int(H), _DTYPE[dtype])
+    if P < 0:
+        raise GblnError("gbln_layernorm_bwd_num_partials", 1)
+    return int(P)
+
+
+def layernorm_bwd(dy, h, weight, mean, rstd, dresidual_out=None, *, dx=None, dwdb_partial=None):
+    """``gbln_layernorm_bwd``.  Returns ``(dx, dwdb_partial, P)``; finish with
+    :func:`layernorm_dwdb_finalize`."""
+    H = dy.shape[-1]
+    T = dy.numel() // H if H else 0
+    P = layernorm_bwd_num_partials(T, H, dy.dtype)
+    if dx is None:
+        dx = torch.empty_like(dy)
+    if dwdb_partial is None:
+        dwdb_partial = torch.empty((max(P, 1), 2 * H), dtype=torch.float32, device=dy.device)
+    st = library().gbln_layernorm_bwd(
+        _dev(dy, "dy"), _opt(dresidual_out, "dresidual_out"), _dev(h, "h"), _dev(weight, "weight"),
+        _dev(mean, "mean"), _dev(rstd, "rstd"), _dev(dx, "dx"), _dev(dwdb_partial, "dwdb_partial"),
+        dwdb_partial.shape[0], T, H, _io(dy), _io(weight), _stream(dy))
+    _check("gbln_layernorm_bwd", st)
+    return dx, dwdb_partial, P
+
+
+def layernorm_dwdb_finalize(dwdb_partial, P, dw=None, db=None, accumulate=False):
+    """``gbln_layernorm_dwdb_finalize``: float32 (dW [H], dB [H])."""
+    H = dwdb_partial.shape[-1] // 2
+    if dw is None:
+        dw = torch.empty(H, dtype=torch.float32, device=dwdb_partial.device)
+    if db is None:
+        db = torch.empty(H, dtype=torch.float32, device=dwdb_partial.device)
+    st = library().gbln_layernorm_dwdb_finalize(
+        _dev(dwdb_partial, "dwdb_partial"), int(P), H, _dev(dw, "dw"), _dev(db, "db"),
+        1 if accumulate else 0, _stream(dwdb_partial))
+    _check("gbln_layernorm_dwdb_finalize", st)
+    return dw, db
 
 
 # ---------------------------------------------------------------------------

@@ -135,6 +135,73 @@ __device__ __forceinline__ float group_sum(float v) {
 }
 
 // ---------------------------------------------------------------------------
+// Row-wise helpers shared by the normalisation kernels.
+// ---------------------------------------------------------------------------
+
+// Load VEC weights (as float) for the 16-byte activation vector at index iv.
+template <typename W, int VEC>
+__device__ __forceinline__ void load_weight(const W* w, int iv, float (&out)[VEC]) {
+  if constexpr (sizeof(W) * VEC == 16) {
+    unpack<VEC>(ld_reuse(w + (size_t)iv * VEC), out);
+  } else {  // float weights with bf16 activations: two 16-byte loads
+    float a[4], b[4];
+    unpack<4>(ld_reuse(w + (size_t)iv * VEC), a);
+    unpack<4>(ld_reuse(w + (size_t)iv * VEC + 4), b);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) { out[e] = a[e]; out[e + 4] = b[e]; }
+  }
+}
+
+// Sum of v over the TPR threads of a row group; identical value in every thread.
+// TPR <= 32: shuffles.  TPR > 32 (one row per block): shuffles + shared memory
+// red[TPR / 32]; safe to call back to back.
+template <int TPR>
+__device__ __forceinline__ float row_sum(float v, float* red) {
+  if constexpr (TPR <= 32) {
+    return group_sum<TPR>(v);
+  } else {
+    v = group_sum<32>(v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();  // red[] may still be read from the previous call
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < TPR / 32; ++i) s += red[i];
+    return s;
+  }
+}
+
+// Fixed-order column sums of a [P, ld] float32 buffer: out[j] = (acc ? out[j] :
+// 0) + sum_p partial[p * ld + j] for j < ncol.  Block (32, kColSumStripes):
+// column j = 32 * blockIdx.x + tx; row stripe ty sums p = ty, ty + stripes, ...
+// in order (loads unrolled so several are in flight; the additions stay in
+// that order), then the stripes are added in order.  Bitwise reproducible.
+constexpr int kColSumStripes = 32;
+
+template <int DUMMY = 0>
+__global__ void __launch_bounds__(32 * kColSumStripes)
+colsum_kernel(const float* __restrict__ partial, int64_t P, int ncol, int ld, float* out,
+              int accumulate) {
+  __shared__ float s[kColSumStripes][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int j = blockIdx.x * 32 + tx;
+  float a = 0.f;
+  if (j < ncol) {
+#pragma unroll 8
+    for (int64_t q = ty; q < P; q += kColSumStripes) a += __ldg(partial + (size_t)q * ld + j);
+  }
+  s[ty][tx] = a;
+  __syncthreads();
+  if (ty == 0 && j < ncol) {
+    float t = 0.f;
+#pragma unroll
+    for (int q = 0; q < kColSumStripes; ++q) t += s[q][tx];
+    out[j] = accumulate ? out[j] + t : t;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // TMA bulk copies (global -> shared) completed on an mbarrier.
 // ---------------------------------------------------------------------------
 

@@ -25,39 +25,6 @@ constexpr int kWarpBlock = 256;      // block of the warp-per-row regime
 constexpr int kMaxVecPerRow = 2048;  // 512 threads x 4 vectors: register-resident limit
 constexpr int kGenericBlock = 256;
 
-// Load VEC weights (as float) for the 16-byte activation vector at index iv.
-template <typename W, int VEC>
-__device__ __forceinline__ void load_weight(const W* w, int iv, float (&out)[VEC]) {
-  if constexpr (sizeof(W) * VEC == 16) {
-    unpack<VEC>(ld_reuse(w + (size_t)iv * VEC), out);
-  } else {  // float weights with bf16 activations: two 16-byte loads
-    float a[4], b[4];
-    unpack<4>(ld_reuse(w + (size_t)iv * VEC), a);
-    unpack<4>(ld_reuse(w + (size_t)iv * VEC + 4), b);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) { out[e] = a[e]; out[e + 4] = b[e]; }
-  }
-}
-
-// Sum of v over the TPR threads of a row group; identical value in every thread.
-// TPR <= 32: shuffles.  TPR > 32 (one row per block): shuffles + shared memory.
-template <int TPR>
-__device__ __forceinline__ float row_sum(float v, float* red) {
-  if constexpr (TPR <= 32) {
-    return group_sum<TPR>(v);
-  } else {
-    v = group_sum<32>(v);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();  // red[] may still be read from the previous row
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < TPR / 32; ++i) s += red[i];
-    return s;
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Forward, vector path.  A row group of TPR threads owns one row; thread l owns
 // the 16-byte vectors l, l + TPR, ..., (VPT of them).  BLOCK / TPR rows per block.
@@ -296,34 +263,6 @@ rms_bwd_generic(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
 }
 
 // ---------------------------------------------------------------------------
-// Finalize: dw[j] = (acc ? dw[j] : 0) + sum_p partial[p, j].  Block (32, 32):
-// column j = 32 * blockIdx.x + tx; row stripe ty sums p = ty, ty + 32, ... in
-// order (loads unrolled so several are in flight; the additions stay in that
-// order), then the 32 stripes are added in order.  Bitwise reproducible.
-// ---------------------------------------------------------------------------
-constexpr int kFinStripes = 32;
-
-__global__ void __launch_bounds__(32 * kFinStripes)
-rms_dw_finalize(const float* __restrict__ partial, int64_t P, int H, float* dw, int accumulate) {
-  __shared__ float s[kFinStripes][33];
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int j = blockIdx.x * 32 + tx;
-  float a = 0.f;
-  if (j < H) {
-#pragma unroll 8
-    for (int64_t q = ty; q < P; q += kFinStripes) a += __ldg(partial + (size_t)q * H + j);
-  }
-  s[ty][tx] = a;
-  __syncthreads();
-  if (ty == 0 && j < H) {
-    float t = 0.f;
-#pragma unroll
-    for (int q = 0; q < kFinStripes; ++q) t += s[q][tx];
-    dw[j] = accumulate ? dw[j] + t : t;
-  }
-}
-
-// ---------------------------------------------------------------------------
 // Launch geometry, shared by forward, backward and num_partials.
 // ---------------------------------------------------------------------------
 struct Geometry {
@@ -531,7 +470,7 @@ extern "C" gbln_status gbln_rmsnorm_dw_finalize(const float* dw_partial, int64_t
   if (!dw || (P > 0 && !dw_partial)) return GBLN_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   const unsigned grid = (unsigned)((H + 31) / 32);
-  rms_dw_finalize<<<grid, 32 * kFinStripes, 0, s>>>(dw_partial, P, (int)H, dw, accumulate ? 1 : 0);
+  colsum_kernel<<<grid, 32 * kColSumStripes, 0, s>>>(dw_partial, P, (int)H, (int)H, dw, accumulate ? 1 : 0);
   return launch_status();
 }
 
@@ -590,7 +529,7 @@ extern "C" gbln_status gbln_rmsnorm_bwd_noalloc(const void* dy, const void* dres
   if (!dw) return GBLN_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   if (T == 0) {  // no rows: dW = 0
-    rms_dw_finalize<<<(unsigned)((H + 31) / 32), 32 * kFinStripes, 0, s>>>(nullptr, 0, (int)H, dw, 0);
+    colsum_kernel<<<(unsigned)((H + 31) / 32), 32 * kColSumStripes, 0, s>>>(nullptr, 0, (int)H, (int)H, dw, 0);
     return launch_status();
   }
   if (!dy || !h || !weight || !rstd || !dx) return GBLN_ERR_INVALID_ARG;
@@ -610,6 +549,6 @@ extern "C" gbln_status gbln_rmsnorm_bwd_noalloc(const void* dy, const void* dres
   else
     st = bwd_typed<bf16, float>(dy, dresidual_out, h, weight, rstd, dx, scratch, P, T, H, s);
   if (st != GBLN_OK) return st;
-  rms_dw_finalize<<<(unsigned)((H + 31) / 32), 32 * kFinStripes, 0, s>>>(scratch, P, (int)H, dw, 0);
+  colsum_kernel<<<(unsigned)((H + 31) / 32), 32 * kColSumStripes, 0, s>>>(scratch, P, (int)H, (int)H, dw, 0);
   return launch_status();
 }

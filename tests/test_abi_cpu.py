@@ -153,6 +153,26 @@ def test_swiglu_rejects(lib):
     assert lib.gbln_swiglu_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 8, F32, None) == OK
 
 
+def test_layernorm_rejects(lib):
+    f = FAKE
+    def fwd(x=f, r=None, w=f, b=None, y=f, ho=None, m=f, rs=f, T=4, H=8, eps=1e-5, io=BF16, wt=BF16):
+        return lib.gbln_layernorm_fwd(x, r, w, b, y, ho, m, rs, T, H, eps, io, wt, None)
+    for kw in ({"x": None}, {"w": None}, {"y": None}, {"m": None}, {"rs": None}, {"r": f},
+               {"T": -1}, {"H": 0}, {"eps": -1.0}, {"eps": float("nan")}, {"io": 4}):
+        assert fwd(**kw) == INVALID, kw
+    assert fwd(io=F32, wt=BF16) == UNSUPPORTED
+    assert fwd(T=0, x=None, w=None, y=None, m=None, rs=None) == OK
+    def bwd(dy=f, h=f, w=f, m=f, rs=f, dx=f, part=f, P=10, T=4, H=8):
+        return lib.gbln_layernorm_bwd(dy, None, h, w, m, rs, dx, part, P, T, H, BF16, BF16, None)
+    for kw in ({"dy": None}, {"h": None}, {"m": None}, {"part": None}, {"P": -1}, {"H": -2}):
+        assert bwd(**kw) == INVALID, kw
+    assert bwd(T=0, dy=None) == OK
+    assert lib.gbln_layernorm_bwd_num_partials(-1, 8, BF16) == -1
+    assert lib.gbln_layernorm_bwd_num_partials(0, 8, BF16) == 0
+    assert lib.gbln_layernorm_dwdb_finalize(f, 2, 8, f, None, 0, None) == INVALID
+    assert lib.gbln_layernorm_dwdb_finalize(None, 2, 8, f, f, 0, None) == INVALID
+
+
 def test_glu_and_act_reject(lib):
     f = FAKE
     assert lib.gbln_glu_fwd(f, f, f, 4, 8, 7, 8, 8, 0, BF16, None) == INVALID  # ld < I

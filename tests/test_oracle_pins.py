@@ -427,3 +427,61 @@ def test_rope_interleaved_equals_complex_multiplication():
     x2 = rng.normal(size=(3, 2, 2))
     p2 = np.array([1, 5, 9])
     assert np.array_equal(oracle.rope_fwd(x2, p2, 1e4, "interleaved"), oracle.rope_fwd(x2, p2, 1e4))
+
+
+# ---------------------------------------------------------------------------
+# LayerNorm
+# ---------------------------------------------------------------------------
+
+def test_layernorm_closed_forms():
+    rng = np.random.default_rng(30)
+    x = rng.normal(size=(6, 20)) * 3 + 5
+    w = 1 + 0.1 * rng.normal(size=20)
+    b = rng.normal(size=20)
+    for eps in (0.0, 1e-5, 0.7):
+        y, h, mean, rstd = oracle.layernorm_fwd(x, None, w, b, eps)
+        n = (y - b) / w
+        var = np.var(x, axis=1)
+        assert np.allclose(np.mean(n, axis=1), 0.0, atol=1e-13)           # zero mean
+        assert np.allclose(np.mean(n * n, axis=1), var / (var + eps), rtol=1e-12)  # unit variance at eps 0
+        assert np.allclose(mean, np.mean(x, axis=1), rtol=1e-15)
+    # shift invariance, and equality with RMSNorm on zero-mean rows
+    y1, *_ = oracle.layernorm_fwd(x, None, w, b, 1e-5)
+    y2, *_ = oracle.layernorm_fwd(x + 123.25, None, w, b, 1e-5)
+    assert np.allclose(y1, y2, rtol=1e-10, atol=1e-10)
+    z = x - np.mean(x, axis=1, keepdims=True)
+    yl, *_ = oracle.layernorm_fwd(z, None, w, None, 1e-5)
+    yr, _, _ = oracle.rmsnorm_fwd(z, None, w, 1e-5)
+    assert np.allclose(yl, yr, rtol=1e-12, atol=1e-13)
+    # one channel: the normalised value is 0, the output is the bias, dx = dres
+    y, _, _, _ = oracle.layernorm_fwd(np.array([[3.0]]), None, np.array([2.0]), np.array([0.5]), 1e-5)
+    assert y[0, 0] == 0.5
+    dx, dw, db = oracle.layernorm_bwd(np.array([[1.5]]), np.array([[0.25]]), np.array([[3.0]]), np.array([2.0]), 1e-5)
+    assert dx[0, 0] == pytest.approx(0.25, abs=1e-15) and dw[0] == 0.0 and db[0] == 1.5
+
+
+@pytest.mark.parametrize("H", [2, 5, 8])
+def test_layernorm_bwd_central_differences(H):
+    rng = np.random.default_rng(31 + H)
+    T, eps, d = 3, 1e-2, 1e-6
+    x = rng.normal(size=(T, H))
+    r = rng.normal(size=(T, H))
+    w = 1 + 0.1 * rng.normal(size=H)
+    b = rng.normal(size=H)
+    dy = rng.normal(size=(T, H))
+    dres = rng.normal(size=(T, H))
+
+    def loss(x, w, b):
+        y, h, _, _ = oracle.layernorm_fwd(x, r, w, b, eps)
+        return float(np.sum(dy * y) + np.sum(dres * h))
+
+    _, h, _, _ = oracle.layernorm_fwd(x, r, w, b, eps)
+    dx, dw, db = oracle.layernorm_bwd(dy, dres, h, w, eps)
+    for arr, grad, which in ((x, dx, "x"), (w, dw, "w"), (b, db, "b")):
+        for idx in np.ndindex(arr.shape):
+            ap = arr.copy(); ap[idx] += d
+            am = arr.copy(); am[idx] -= d
+            args_p = {"x": x, "w": w, "b": b}; args_p[which] = ap
+            args_m = {"x": x, "w": w, "b": b}; args_m[which] = am
+            fd = (loss(args_p["x"], args_p["w"], args_p["b"]) - loss(args_m["x"], args_m["w"], args_m["b"])) / (2 * d)
+            assert grad[idx] == pytest.approx(fd, rel=1e-6, abs=1e-8), (which, idx)
