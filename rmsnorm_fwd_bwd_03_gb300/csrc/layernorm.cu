@@ -20,7 +20,6 @@ namespace gbln {
 namespace {
 
 constexpr int kLnWarpBlock = 256;
-constexpr int kLnMaxVecPerRow = 2048;
 constexpr int kLnGenericBlock = 256;
 
 // ---------------------------------------------------------------------------
@@ -306,16 +305,21 @@ struct LnGeometry {
   int tpr, vpt, block, rpc, bps;
 };
 
-LnGeometry ln_geometry(int64_t H, size_t io_size) {
+// Forward: up to 4 vectors per thread (~50 registers).  Backward: up to 2, since
+// each thread also carries dW and dB accumulators for its columns (~100
+// registers at 2 vectors, 150-165 at 4, which would leave too few resident
+// blocks for the persistent grid).
+LnGeometry ln_geometry(int64_t H, size_t io_size, bool bwd) {
   LnGeometry g{};
+  const int max_vpt = bwd ? 2 : 4;
   const int64_t row_bytes = H * (int64_t)io_size;
   const int64_t nvec = row_bytes / 16;
-  if (row_bytes % 16 != 0 || nvec > kLnMaxVecPerRow) {
+  if (row_bytes % 16 != 0 || nvec > 512LL * max_vpt) {
     g.vec = false; g.tpr = kLnGenericBlock; g.vpt = 0; g.block = kLnGenericBlock; g.rpc = 1; g.bps = 4;
     return g;
   }
   g.vec = true;
-  if (nvec <= 128) {
+  if (nvec <= 32LL * max_vpt) {
     g.tpr = 32;
     g.vpt = nvec <= 32 ? 1 : (nvec <= 64 ? 2 : 4);
     g.block = kLnWarpBlock;
@@ -323,9 +327,9 @@ LnGeometry ln_geometry(int64_t H, size_t io_size) {
     g.bps = 2;
   } else {
     int tpr = 64;
-    while ((int64_t)tpr * 4 < nvec) tpr *= 2;  // <= 512 by kLnMaxVecPerRow
+    while ((int64_t)tpr * max_vpt < nvec) tpr *= 2;  // <= 512
     g.tpr = tpr;
-    g.vpt = 4;
+    g.vpt = max_vpt;
     g.block = tpr;
     g.rpc = 1;
     g.bps = 512 / tpr > 0 ? 512 / tpr : 1;
@@ -360,7 +364,7 @@ gbln_status ln_fwd_typed(const void* x, const void* r, const void* w, const void
                          void* hout, float* mean, float* rstd, int64_t rows, int64_t H, float eps,
                          cudaStream_t s) {
   const bool res = r != nullptr, bias = b != nullptr;
-  const LnGeometry g = ln_geometry(H, sizeof(T));
+  const LnGeometry g = ln_geometry(H, sizeof(T), false);
   const bool vec = g.vec && aligned16(x) && aligned16(w) && aligned16(y) &&
                    (!bias || aligned16(b)) && (!res || (aligned16(r) && aligned16(hout)));
   const float inv_H = 1.0f / (float)H;
@@ -408,7 +412,7 @@ gbln_status ln_bwd_typed(const void* dy, const void* dr, const void* h, const vo
                          const float* mean, const float* rstd, void* dx, float* partial, int64_t P,
                          int64_t rows, int64_t H, cudaStream_t s) {
   const bool dres = dr != nullptr;
-  const LnGeometry g = ln_geometry(H, sizeof(T));
+  const LnGeometry g = ln_geometry(H, sizeof(T), true);
   const bool vec = g.vec && aligned16(dy) && aligned16(h) && aligned16(w) && aligned16(dx) &&
                    aligned16(partial) && (!dres || aligned16(dr));
   const float inv_H = 1.0f / (float)H;
@@ -425,14 +429,13 @@ gbln_status ln_bwd_typed(const void* dy, const void* dr, const void* h, const vo
   }
   if (g.tpr == 32) {
     if (g.vpt == 1) ln_bwd_vec_launch<T, W, 32, 1, kLnWarpBlock>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s);
-    else if (g.vpt == 2) ln_bwd_vec_launch<T, W, 32, 2, kLnWarpBlock>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s);
-    else ln_bwd_vec_launch<T, W, 32, 4, kLnWarpBlock>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s);
+    else ln_bwd_vec_launch<T, W, 32, 2, kLnWarpBlock>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s);
   } else {
     switch (g.tpr) {
-      case 64: ln_bwd_vec_launch<T, W, 64, 4, 64>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
-      case 128: ln_bwd_vec_launch<T, W, 128, 4, 128>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
-      case 256: ln_bwd_vec_launch<T, W, 256, 4, 256>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
-      default: ln_bwd_vec_launch<T, W, 512, 4, 512>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
+      case 64: ln_bwd_vec_launch<T, W, 64, 2, 64>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
+      case 128: ln_bwd_vec_launch<T, W, 128, 2, 128>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
+      case 256: ln_bwd_vec_launch<T, W, 256, 2, 256>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
+      default: ln_bwd_vec_launch<T, W, 512, 2, 512>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
     }
   }
   return launch_status();
@@ -476,7 +479,7 @@ extern "C" int64_t gbln_layernorm_bwd_num_partials(int64_t T, int64_t H, gbln_dt
   if (T == 0) return 0;
   const int sms = sm_count();
   if (sms <= 0) return -1;
-  return ln_partials_for(T, ln_geometry(H, dtype_size(io)), sms);
+  return ln_partials_for(T, ln_geometry(H, dtype_size(io), true), sms);
 }
 
 extern "C" gbln_status gbln_layernorm_bwd(const void* dy, const void* dresidual_out,
@@ -491,7 +494,7 @@ extern "C" gbln_status gbln_layernorm_bwd(const void* dy, const void* dresidual_
   if (!dy || !h || !weight || !mean || !rstd || !dx || !dwdb_partial) return GBLN_ERR_INVALID_ARG;
   const int sms = sm_count();
   if (sms <= 0) return GBLN_ERR_CUDA;
-  const int64_t P = ln_partials_for(T, ln_geometry(H, dtype_size(io)), sms);
+  const int64_t P = ln_partials_for(T, ln_geometry(H, dtype_size(io), true), sms);
   if (P_cap < P) return GBLN_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
   if (io == GBLN_F32)
