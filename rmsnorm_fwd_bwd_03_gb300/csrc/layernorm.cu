@@ -13,6 +13,8 @@
 // groups in a fixed order and written as one [dW | dB] partial row per block;
 // a second launch sums the partial rows in a fixed order (bitwise reproducible).
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace gbln {
@@ -262,6 +264,97 @@ ln_bwd_vec(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
   }
 }
 
+// Backward, vector path for one row per block (TPR = BLOCK > 32): the dW and
+// dB accumulators live in shared memory, slot k of thread t at acc[k * TPR + t]
+// (consecutive threads hit consecutive banks), instead of in registers, so the
+// kernel fits 64 registers and 1024 threads stay resident per SM.
+template <typename T, typename W, int TPR, int VPT, bool DRES>
+__global__ void __launch_bounds__(TPR, 1024 / TPR)
+ln_bwd_cta(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
+           const float* __restrict__ mean, const float* __restrict__ rstd, T* dx,
+           float* __restrict__ partial, int64_t rows, int H, float inv_H) {
+  constexpr int VEC = VecOf<T>::N;
+  constexpr int NACC = VPT * VEC;  // accumulator slots per thread and gradient
+  extern __shared__ float acc[];   // [2 * NACC][TPR]: dW slots, then dB slots
+  __shared__ float red[TPR / 32];
+  const int l = threadIdx.x;
+  const int nvec = H / VEC;
+  const int64_t P = gridDim.x, p = blockIdx.x;
+  const int64_t r0 = p * rows / P, r1 = (p + 1) * rows / P;
+#pragma unroll
+  for (int k = 0; k < 2 * NACC; ++k) acc[k * TPR + l] = 0.f;
+
+  for (int64_t row = r0; row < r1; ++row) {  // same trip count in every thread
+    const size_t base = (size_t)row * H;
+    uint4 dya[VPT], ha[VPT], dra[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int iv = l + v * TPR;
+      if (iv < nvec) {
+        dya[v] = ld_stream(dy + base + (size_t)iv * VEC);
+        ha[v] = ld_stream(h + base + (size_t)iv * VEC);
+        if constexpr (DRES) dra[v] = ld_stream(dres + base + (size_t)iv * VEC);
+      }
+    }
+    const float mu = mean[row], rs = rstd[row];
+    float sg = 0.f, sgn = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int iv = l + v * TPR;
+      if (iv < nvec) {
+        float d[VEC], n[VEC], wv[VEC];
+        unpack<VEC>(dya[v], d);
+        unpack<VEC>(ha[v], n);
+        load_weight<W, VEC>(w, iv, wv);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          n[e] = (n[e] - mu) * rs;
+          const float gg = d[e] * wv[e];
+          sg += gg;
+          sgn = fmaf(gg, n[e], sgn);
+          float* aw = acc + (v * VEC + e) * TPR + l;
+          float* ab = acc + (NACC + v * VEC + e) * TPR + l;
+          *aw = fmaf(d[e], n[e], *aw);
+          *ab += d[e];
+        }
+      }
+    }
+    const float mg = row_sum<TPR>(sg, red) * inv_H;
+    const float mgn = row_sum<TPR>(sgn, red) * inv_H;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int iv = l + v * TPR;
+      if (iv < nvec) {
+        float d[VEC], n[VEC], wv[VEC], o[VEC];
+        unpack<VEC>(dya[v], d);
+        unpack<VEC>(ha[v], n);
+        load_weight<W, VEC>(w, iv, wv);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] = rs * (d[e] * wv[e] - mg - ((n[e] - mu) * rs) * mgn);
+        if constexpr (DRES) {
+          float d2[VEC];
+          unpack<VEC>(dra[v], d2);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) o[e] += d2[e];
+        }
+        st_vec(dx + base + (size_t)iv * VEC, pack<T, VEC>(o));
+      }
+    }
+  }
+  float* prow = partial + (size_t)p * 2 * H;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int iv = l + v * TPR;
+    if (iv < nvec) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        prow[iv * VEC + e] = acc[(v * VEC + e) * TPR + l];
+        prow[H + iv * VEC + e] = acc[(NACC + v * VEC + e) * TPR + l];
+      }
+    }
+  }
+}
+
 // Backward, element-wise path: P blocks over contiguous row chunks, one row at
 // a time; thread t owns columns t, t + 256, ... of the partial row.
 template <typename T, typename W, bool DRES>
@@ -302,6 +395,7 @@ ln_bwd_generic(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
 // ---------------------------------------------------------------------------
 struct LnGeometry {
   bool vec;
+  bool smem_acc;  // backward with shared-memory accumulators (ln_bwd_cta)
   int tpr, vpt, block, rpc, bps;
 };
 
@@ -319,7 +413,13 @@ LnGeometry ln_geometry(int64_t H, size_t io_size, bool bwd) {
     return g;
   }
   g.vec = true;
-  if (nvec <= 32LL * max_vpt) {
+  // Backward (2 vectors per thread): rows of up to 64 vectors take a warp per
+  // row and rows of up to 128 a 64-thread block per row, both with register
+  // accumulators; wider rows one block per row with the accumulators in shared
+  // memory (ln_bwd_cta: at most 64 registers, 1024 threads per SM).  Blocks per
+  // SM set P, the number of [dW | dB] partial rows.
+  const int64_t warp_limit = bwd ? 64 : 32LL * max_vpt;
+  if (nvec <= warp_limit) {
     g.tpr = 32;
     g.vpt = nvec <= 32 ? 1 : (nvec <= 64 ? 2 : 4);
     g.block = kLnWarpBlock;
@@ -332,7 +432,9 @@ LnGeometry ln_geometry(int64_t H, size_t io_size, bool bwd) {
     g.vpt = max_vpt;
     g.block = tpr;
     g.rpc = 1;
-    g.bps = 512 / tpr > 0 ? 512 / tpr : 1;
+    g.smem_acc = bwd && nvec > 128;
+    const int threads_per_sm = g.smem_acc ? 1024 : 512;
+    g.bps = threads_per_sm / tpr > 0 ? threads_per_sm / tpr : 1;
   }
   return g;
 }
@@ -407,6 +509,35 @@ void ln_bwd_vec_launch(bool dres, unsigned P, const void* dy, const void* dr, co
         (const T*)dy, nullptr, (const T*)h, (const W*)w, mean, rstd, (T*)dx, partial, rows, H, inv_H);
 }
 
+template <typename T, typename W, int TPR, int VPT>
+gbln_status ln_bwd_cta_launch(bool dres, unsigned P, const void* dy, const void* dr, const void* h,
+                              const void* w, const float* mean, const float* rstd, void* dx,
+                              float* partial, int64_t rows, int H, float inv_H, cudaStream_t s) {
+  constexpr int VEC = VecOf<T>::N;
+  const size_t smem = (size_t)2 * VPT * VEC * TPR * sizeof(float);
+  static std::atomic<uint64_t> attr_done{0};  // one bit per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return GBLN_ERR_CUDA; }
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+    if (cudaFuncSetAttribute(ln_bwd_cta<T, W, TPR, VPT, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(ln_bwd_cta<T, W, TPR, VPT, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+      cudaGetLastError();
+      return GBLN_ERR_CUDA;
+    }
+    attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  if (dres)
+    ln_bwd_cta<T, W, TPR, VPT, true><<<P, TPR, smem, s>>>(
+        (const T*)dy, (const T*)dr, (const T*)h, (const W*)w, mean, rstd, (T*)dx, partial, rows, H, inv_H);
+  else
+    ln_bwd_cta<T, W, TPR, VPT, false><<<P, TPR, smem, s>>>(
+        (const T*)dy, nullptr, (const T*)h, (const W*)w, mean, rstd, (T*)dx, partial, rows, H, inv_H);
+  return GBLN_OK;
+}
+
 template <typename T, typename W>
 gbln_status ln_bwd_typed(const void* dy, const void* dr, const void* h, const void* w,
                          const float* mean, const float* rstd, void* dx, float* partial, int64_t P,
@@ -430,13 +561,17 @@ gbln_status ln_bwd_typed(const void* dy, const void* dr, const void* h, const vo
   if (g.tpr == 32) {
     if (g.vpt == 1) ln_bwd_vec_launch<T, W, 32, 1, kLnWarpBlock>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s);
     else ln_bwd_vec_launch<T, W, 32, 2, kLnWarpBlock>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s);
+  } else if (!g.smem_acc) {
+    ln_bwd_vec_launch<T, W, 64, 2, 64>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s);
   } else {
+    gbln_status st = GBLN_OK;
     switch (g.tpr) {
-      case 64: ln_bwd_vec_launch<T, W, 64, 2, 64>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
-      case 128: ln_bwd_vec_launch<T, W, 128, 2, 128>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
-      case 256: ln_bwd_vec_launch<T, W, 256, 2, 256>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
-      default: ln_bwd_vec_launch<T, W, 512, 2, 512>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
+      case 64: st = ln_bwd_cta_launch<T, W, 64, 2>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
+      case 128: st = ln_bwd_cta_launch<T, W, 128, 2>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
+      case 256: st = ln_bwd_cta_launch<T, W, 256, 2>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
+      default: st = ln_bwd_cta_launch<T, W, 512, 2>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
     }
+    if (st != GBLN_OK) return st;
   }
   return launch_status();
 }
