@@ -64,6 +64,15 @@ __all__ = [
     "glu_bwd",
     "positions_from_doc_lengths",
     "positions_from_cu_seqlens",
+    "E4M3_MAX",
+    "round_to_e4m3",
+    "e4m3_encode",
+    "e4m3_decode",
+    "mx_scale_exponent",
+    "mxfp8_quantize",
+    "mxfp8_dequantize",
+    "rmsnorm_fwd_mxfp8",
+    "glu_fwd_mxfp8",
 ]
 
 
@@ -389,3 +398,127 @@ def positions_from_cu_seqlens(cu_seqlens):
     """Same, from cumulative document boundaries ``cu_seqlens`` (cu[0] = 0, cu[-1] = T)."""
     cu = np.asarray(cu_seqlens, dtype=np.int64)
     return positions_from_doc_lengths(cu[1:] - cu[:-1])
+
+
+# ---------------------------------------------------------------------------
+# MXFP8 output: the FP8 operand layout of the next projection GEMM
+# ("Kernels（自定义内核）": fusing the producer of a tensor with its consumer's
+#  input conversion saves a pass over HBM; the format itself is the OCP
+#  Microscaling Formats (MX) v1.0 specification's MXFP8 with E4M3 elements:
+#  blocks of 32 consecutive values share one power-of-two scale stored as an
+#  E8M0 byte).  Blocks run along the last axis (the GEMM's reduction axis).
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0        # largest finite E4M3 magnitude: 1.75 * 2**8
+_E4M3_EMIN = -6         # exponent of the smallest normal, 2**-6
+_E4M3_MBITS = 3         # stored mantissa bits
+_E4M3_EMAX = 8          # exponent of the largest normal (the MX "emax_elem")
+_E8M0_BIAS = 127
+MX_BLOCK = 32
+
+
+def round_to_e4m3(a):
+    """Round float64 values to the nearest E4M3 value, ties to even, saturating.
+
+    E4M3 (as used by MXFP8): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+    bits, no infinities.  Normal values are ``(1 + m/8) * 2**e`` for e in
+    [-6, 8]; below 2**-6 the spacing is the subnormal quantum 2**-9.  Written from
+    that definition: the spacing at |a| is ``2**(max(floor(log2|a|), -6) - 3)``;
+    divide by it, round half to even, multiply back.  Magnitudes that round
+    beyond 448 become 448 (saturation); NaN stays NaN.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    mag = np.abs(a)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        _, e2 = np.frexp(mag)           # mag = f * 2**e2 with 0.5 <= f < 1
+    e = np.maximum(e2 - 1, _E4M3_EMIN)  # floor(log2 mag) for mag > 0, clamped at the subnormal range
+    quantum = np.ldexp(1.0, e - _E4M3_MBITS)
+    r = np.rint(mag / quantum) * quantum
+    r = np.where(mag == 0, 0.0, r)
+    r = np.minimum(r, E4M3_MAX)
+    return np.where(np.isnan(a), np.nan, np.copysign(r, a))
+
+
+def e4m3_encode(v):
+    """Bit pattern (uint8) of E4M3 values ``v`` (which must already be E4M3 values)."""
+    v = np.asarray(v, dtype=np.float64)
+    sign = np.signbit(v).astype(np.uint8) << 7
+    mag = np.abs(v)
+    _, e2 = np.frexp(mag)
+    e = e2 - 1
+    normal = mag >= 2.0 ** _E4M3_EMIN
+    # normal: exponent field e + 7, mantissa (mag / 2**e - 1) * 8
+    ef = np.where(normal, e + 7, 0)
+    mf = np.where(normal, np.rint((np.ldexp(mag, -e) - 1.0) * 8.0),
+                  np.rint(mag / 2.0 ** (_E4M3_EMIN - _E4M3_MBITS)))
+    code = sign | (ef.astype(np.uint8) << 3) | mf.astype(np.uint8)
+    return np.where(np.isnan(v), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def e4m3_decode(code):
+    """E4M3 bit patterns (uint8) to float64: sign, exponent field E, mantissa M;
+    E = 0 gives ``M * 2**-9``, otherwise ``(1 + M/8) * 2**(E - 7)``; 0x7F / 0xFF are NaN."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    E = (c >> 3) & 0xF
+    M = c & 0x7
+    val = np.where(E == 0, M * 2.0 ** (_E4M3_EMIN - _E4M3_MBITS),
+                   (1.0 + M / 8.0) * np.ldexp(1.0, E - 7))
+    val = s * val
+    return np.where((E == 15) & (M == 7), np.nan, val)
+
+
+def mx_scale_exponent(amax):
+    """Shared exponent of an MX block with largest magnitude ``amax``.
+
+    The MX conversion takes ``floor(log2(amax)) - emax_elem`` (emax_elem = 8 for
+    E4M3), so the block's largest value lands in E4M3's top binade; E8M0 holds
+    exponents -127..127, and an all-zero block takes the smallest, -127.
+    """
+    amax = np.asarray(amax, dtype=np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        _, e2 = np.frexp(amax)
+    se = np.where(amax > 0, (e2 - 1) - _E4M3_EMAX, -_E8M0_BIAS)
+    return np.clip(se, -_E8M0_BIAS, _E8M0_BIAS).astype(np.int64)
+
+
+def mxfp8_quantize(v, block=MX_BLOCK):
+    """MXFP8 (E4M3) quantization of ``v`` [..., N] in blocks of ``block`` along the last axis.
+
+    Returns ``(codes, scales)``: codes uint8 [..., N] (E4M3 bit patterns of
+    ``round_to_e4m3(v / 2**se)``) and scales uint8 [..., N / block] (E8M0:
+    ``se + 127``), with ``se = mx_scale_exponent(max |v| over the block)``.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    n = v.shape[-1]
+    if n % block:
+        raise ValueError("the last axis must be a multiple of the block size")
+    vb = v.reshape(v.shape[:-1] + (n // block, block))
+    se = mx_scale_exponent(np.max(np.abs(vb), axis=-1))
+    q = round_to_e4m3(vb / np.ldexp(1.0, se)[..., None])
+    return e4m3_encode(q).reshape(v.shape), (se + _E8M0_BIAS).astype(np.uint8)
+
+
+def mxfp8_dequantize(codes, scales, block=MX_BLOCK):
+    """Values of an MXFP8 tensor: ``e4m3_decode(code) * 2**(scale - 127)`` per block."""
+    c = np.asarray(codes)
+    n = c.shape[-1]
+    vals = e4m3_decode(c).reshape(c.shape[:-1] + (n // block, block))
+    se = np.asarray(scales, dtype=np.int64) - _E8M0_BIAS
+    return (vals * np.ldexp(1.0, se)[..., None]).reshape(c.shape)
+
+
+def rmsnorm_fwd_mxfp8(x, residual, weight, eps, io=None):
+    """RMSNorm forward whose output y is also delivered as MXFP8 (blocks along H).
+
+    Returns ``(codes, scales, y, h, rstd)``: ``y, h, rstd`` as :func:`rmsnorm_fwd`
+    (y exact, before any rounding) and ``codes, scales = mxfp8_quantize(y)``.
+    """
+    y, h, rstd = rmsnorm_fwd(x, residual, weight, eps, io)
+    codes, scales = mxfp8_quantize(y)
+    return codes, scales, y, h, rstd
+
+
+def glu_fwd_mxfp8(name, gate, up):
+    """Gated unit forward delivered as MXFP8: ``mxfp8_quantize(act(gate) * up)``."""
+    return mxfp8_quantize(glu_fwd(name, gate, up))

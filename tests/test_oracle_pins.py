@@ -485,3 +485,149 @@ def test_layernorm_bwd_central_differences(H):
             args_m = {"x": x, "w": w, "b": b}; args_m[which] = am
             fd = (loss(args_p["x"], args_p["w"], args_p["b"]) - loss(args_m["x"], args_m["w"], args_m["b"])) / (2 * d)
             assert grad[idx] == pytest.approx(fd, rel=1e-6, abs=1e-8), (which, idx)
+
+
+# ---------------------------------------------------------------------------
+# MXFP8 (E4M3 elements, E8M0 block scales)
+# ---------------------------------------------------------------------------
+
+def _mx_golden():
+    rounds, blocks = [], []
+    with open(os.path.join(GOLDEN, "e4m3_mx.txt"), encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            tag, *vals = line.split()
+            (rounds if tag == "round" else blocks).append(vals)
+    return rounds, blocks
+
+
+def test_e4m3_hand_cases():
+    rounds, _ = _mx_golden()
+    assert len(rounds) >= 15
+    for num, den, enum, eden, code in rounds:
+        v = int(num) / int(den)
+        got = oracle.round_to_e4m3(np.array([v]))[0]
+        assert got == int(enum) / int(eden), (v, got)
+        assert oracle.e4m3_encode(np.array([got]))[0] == int(code, 16), (v, got)
+
+
+def test_mx_block_hand_cases():
+    _, blocks = _mx_golden()
+    for an, ad, vn, vd, se, sbyte, code0 in blocks:
+        amax, v0 = int(an) / int(ad), int(vn) / int(vd)
+        blk = np.zeros((1, 32))
+        blk[0, 0] = v0
+        blk[0, 17] = -amax  # the block maximum is a magnitude
+        codes, scales = oracle.mxfp8_quantize(blk)
+        assert oracle.mx_scale_exponent(np.array([amax]))[0] == int(se)
+        assert scales[0, 0] == int(sbyte, 16)
+        assert codes[0, 0] == int(code0, 16)
+
+
+def test_e4m3_format_constants():
+    vals = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    finite = vals[~np.isnan(vals)]
+    assert np.isnan(vals).sum() == 2                    # 0x7f and 0xff only
+    assert finite.max() == 448.0 and finite.min() == -448.0
+    pos = finite[finite > 0]
+    assert pos.min() == 2.0 ** -9                        # smallest subnormal
+    assert np.sort(pos)[7] == 2.0 ** -6                  # 7 subnormals, then the smallest normal
+    assert len(np.unique(finite)) == 253                 # +0 and -0 compare equal
+    # every finite code decodes to a value that encodes back to the same code
+    codes = np.arange(256, dtype=np.uint8)[~np.isnan(vals)]
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_decode(codes)), codes)
+
+
+def test_e4m3_rounding_matches_torch_cast_in_range():
+    # torch's float8_e4m3fn cast (round to nearest even) is an independent
+    # implementation; it does not saturate, so compare inside the finite range,
+    # including every midpoint between neighbouring positive and negative values.
+    rng = np.random.default_rng(41)
+    v = rng.standard_normal(100_000) * np.exp(rng.uniform(-14, 6.5, 100_000))
+    grid = np.sort(oracle.e4m3_decode(np.arange(256, dtype=np.uint8)))
+    grid = grid[~np.isnan(grid)]
+    mids = (grid[1:] + grid[:-1]) / 2
+    v = np.concatenate([v, mids, grid])
+    v = v[np.abs(v) <= 448.0]
+    ref = torch.tensor(v, dtype=torch.float64).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.round_to_e4m3(v)
+    assert np.array_equal(np.nan_to_num(got), np.nan_to_num(ref))
+
+
+def test_e4m3_rounding_error_bound_and_saturation():
+    rng = np.random.default_rng(43)
+    v = rng.standard_normal(50_000) * np.exp(rng.uniform(-10, 6, 50_000))
+    q = oracle.round_to_e4m3(v)
+    mag = np.abs(v)
+    # half a spacing: 2**(floor(log2|v|) - 4) in the normal range, 2**-10 below it
+    e = np.floor(np.log2(np.maximum(mag, 2.0 ** -6)))
+    half = np.ldexp(1.0, (e - 4).astype(int))
+    inside = mag <= 448.0
+    assert np.all(np.abs(q - v)[inside] <= half[inside])
+    assert np.all(np.abs(q[~inside]) == 448.0)
+    assert np.all(np.sign(q[q != 0]) == np.sign(v[q != 0]))
+
+
+def test_mxfp8_block_structure():
+    # Blocks run along the last axis: scaling one block changes only its own
+    # scale byte (by the power of two) and leaves every code unchanged.
+    rng = np.random.default_rng(47)
+    v = rng.standard_normal((3, 96))
+    c0, s0 = oracle.mxfp8_quantize(v)
+    assert c0.shape == (3, 96) and s0.shape == (3, 3)
+    w = v.copy()
+    w[1, 32:64] *= 8.0
+    c1, s1 = oracle.mxfp8_quantize(w)
+    assert np.array_equal(c1, c0)
+    assert s1[1, 1] == s0[1, 1] + 3
+    s1[1, 1] = s0[1, 1]
+    assert np.array_equal(s1, s0)
+    # each block's largest magnitude lands in E4M3's top binade [256, 448]
+    deq = oracle.mxfp8_dequantize(c0, s0)
+    for t in range(3):
+        for b in range(3):
+            blk = v[t, 32 * b:32 * (b + 1)]
+            k = int(np.argmax(np.abs(blk)))
+            top = abs(oracle.e4m3_decode(c0[t, 32 * b + k]))
+            assert 256.0 <= top <= 448.0
+    # dequantized values are within half an E4M3 spacing (relative 2**-4) of the inputs,
+    # unless saturated at the top of the range
+    rel = np.abs(deq - v) / np.abs(v)
+    sat = np.abs(oracle.e4m3_decode(c0)) == 448.0
+    small = np.abs(oracle.e4m3_decode(c0)) < 2.0 ** -6
+    assert np.all(rel[~sat & ~small] <= 2.0 ** -4)
+
+
+def test_mxfp8_zero_block_and_scale_clamps():
+    codes, scales = oracle.mxfp8_quantize(np.zeros((1, 32)))
+    assert np.all(codes == 0) and scales[0, 0] == 0
+    assert oracle.mx_scale_exponent(np.array([2.0 ** -140]))[0] == -127
+    assert oracle.mx_scale_exponent(np.array([2.0 ** 140]))[0] == 127
+
+
+def test_rmsnorm_fwd_mxfp8_is_quantized_rmsnorm():
+    rng = np.random.default_rng(53)
+    x = rng.standard_normal((4, 64))
+    r = rng.standard_normal((4, 64))
+    w = 1 + 0.1 * rng.standard_normal(64)
+    codes, scales, y, h, rstd = oracle.rmsnorm_fwd_mxfp8(x, r, w, 1e-6, "bf16")
+    y2, h2, rstd2 = oracle.rmsnorm_fwd(x, r, w, 1e-6, "bf16")
+    assert np.array_equal(y, y2) and np.array_equal(h, h2) and np.array_equal(rstd, rstd2)
+    c2, s2 = oracle.mxfp8_quantize(y2)
+    assert np.array_equal(codes, c2) and np.array_equal(scales, s2)
+    # y = w * h * rstd: with w == 1 and eps = 0 every row has unit RMS, so the
+    # dequantized rows have RMS 1 to within the E4M3 relative error
+    c3, s3, *_ = oracle.rmsnorm_fwd_mxfp8(x, None, np.ones(64), 0.0)
+    deq = oracle.mxfp8_dequantize(c3, s3)
+    assert np.allclose(np.sqrt(np.mean(deq ** 2, axis=1)), 1.0, rtol=2.0 ** -4)
+
+
+def test_glu_fwd_mxfp8_is_quantized_glu():
+    rng = np.random.default_rng(59)
+    g = rng.standard_normal((2, 64))
+    u = rng.standard_normal((2, 64))
+    codes, scales = oracle.glu_fwd_mxfp8("silu", g, u)
+    c2, s2 = oracle.mxfp8_quantize(g / (1 + np.exp(-g)) * u)
+    assert np.array_equal(codes, c2) and np.array_equal(scales, s2)
