@@ -388,7 +388,8 @@ def run_single_op(args, wl, device):
     gbs = alg / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
     print(json.dumps({"op": args.op, "workload": wl.name, "tokens": wl.T, "launches": args.steps,
                       "ms_per_launch": ms, "alg_bytes": alg, "GB/s": round(gbs, 1),
-                      "frac": round(gbs / peak, 4), "peak": peak, "peak_kind": f"of {peak_kind}"}))
+                      "frac": round(gbs / peak, 4), "peak": peak, "peak_kind": f"of {peak_kind}",
+                      "device_error_word": step.gb.device_error()}))
 
 
 def run_next_ops(args, wl, device):
@@ -682,6 +683,8 @@ def main():
         line["e2e"] = e2e_pipelined(wl, device, ksteps, args.warmup, world, seed=rank)
         line["gpu_launches_e2e"] = nk * ksteps
 
+    # Bit 1 is set by a kernel whose bounded wait on its own copies ran out.
+    line["device_error_word"] = step.gb.device_error()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(wl, 256, args.cpu_seconds)
     if rank == 0:
