@@ -394,7 +394,8 @@ def run_single_op(args, wl, device):
 
 def run_next_ops(args, wl, device):
     """Time the operators beyond the step (gated units with other activations and
-    packed layouts, plain activations, strided / interleaved RoPE, LayerNorm) at
+    packed layouts, plain activations, strided / interleaved RoPE, LayerNorm,
+    MXFP8 outputs of the RMSNorm and SwiGLU forwards) at
     the workload's widths: K launches each, CUDA events around each launch, L2
     flushed in between.  One JSON line with per-operator time and GB/s."""
     import rmsnorm_fwd_bwd_03_gb300 as gb
@@ -450,6 +451,18 @@ def run_next_ops(args, wl, device):
     ops["layernorm_fwd"] = (lib.gbln_layernorm_fwd, (p(xl), p(rl), p(wgt), p(bias), p(yl), p(hl), p(mean), p(rstd), T, H, wl.eps, io, io, s), 4 * T * H * b + 8 * T + 2 * H * b)
     ops["layernorm_bwd"] = (lib.gbln_layernorm_bwd, (p(dyl), p(drl), p(hl), p(wgt), p(mean), p(rstd), p(dxl), p(part), P, T, H, io, io, s), 4 * T * H * b + 8 * T + H * b)
     ops["layernorm_dwdb_finalize"] = (lib.gbln_layernorm_dwdb_finalize, (p(part), P, H, p(dwl), p(dbl), 0, s), 0)
+
+    # MXFP8 outputs for the next GEMM: RMSNorm (+ residual) writing h, rstd and
+    # y as E4M3 codes + one scale byte per 32 values (with and without the io copy
+    # of y), and the packed SwiGLU forward writing only the MXFP8 result.
+    if H % 32 == 0 and I % 32 == 0:
+        yq, ysc = torch.empty(T, H, dtype=torch.uint8, device=device), torch.empty(T, H // 32, dtype=torch.uint8, device=device)
+        wr = (1 + 0.1 * torch.randn(H, generator=g, device=device)).to(dt)
+        mx_rms = 2 * T * H * b + T * H * b + T * H + T * H // 32 + 4 * T + H * b
+        ops["rmsnorm_fwd_mxfp8"] = (lib.gbln_rmsnorm_fwd_mxfp8, (p(xl), p(rl), p(wr), None, p(yq), p(ysc), p(hl), p(rstd), T, H, wl.eps, io, io, s), mx_rms)
+        ops["rmsnorm_fwd_mxfp8_and_y"] = (lib.gbln_rmsnorm_fwd_mxfp8, (p(xl), p(rl), p(wr), p(yl), p(yq), p(ysc), p(hl), p(rstd), T, H, wl.eps, io, io, s), mx_rms + T * H * b)
+        gq, gsc = torch.empty(T, I, dtype=torch.uint8, device=device), torch.empty(T, I // 32, dtype=torch.uint8, device=device)
+        ops["swiglu_fwd_packed_mxfp8"] = (lib.gbln_glu_fwd_mxfp8, (p(packed), p(packed) + I * b, p(gq), p(gsc), T, I, 2 * I, 2 * I, gb.ACT["silu"], io, s), 2 * T * I * b + T * I + T * I // 32)
 
     flush = L2Flush(device)
     peak, peak_kind = _measured_peak()

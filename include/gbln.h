@@ -3,7 +3,8 @@
  *
  * Operators: RMSNorm with fused residual add (forward, backward, weight-gradient
  * finalize), rotary position embedding on Q and K (forward, backward, cos/sin
- * table, per-document positions) and SwiGLU (forward, backward).
+ * table, per-document positions) and SwiGLU (forward, backward); LayerNorm,
+ * other gated and plain activations, and MXFP8 outputs for the next GEMM.
  *
  * Sources that name these operators (they print no formulas; the standard
  * definitions are used and written out at each entry point):
@@ -365,6 +366,51 @@ gbln_status gbln_act_fwd(const void* x, void* y, int64_t n, gbln_act act, gbln_d
 /* dx = dy * f'(x) over n contiguous elements; dx may alias dy or x. */
 gbln_status gbln_act_bwd(const void* dy, const void* x, void* dx, int64_t n, gbln_act act,
                          gbln_dtype io, gbln_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* MXFP8 outputs for the next projection GEMM ([HF] Kernels intro: fusing a    */
+/* producer with its consumer's input conversion saves an HBM pass)            */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * MXFP8 as defined by the OCP Microscaling Formats (MX) v1.0 specification:
+ * blocks of 32 consecutive values of a row share one scale 2^e, stored as an
+ * E8M0 byte (e + 127); each value is stored as an E4M3 byte (1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits; largest finite 448).  Here
+ *   e     = floor(log2(max |v| over the block)) - 8, clamped to [-127, 127]
+ *           (-127 for an all-zero block),
+ *   code  = E4M3(v / 2^e), rounded to nearest even, saturating to +-448.
+ * Blocks run along the last axis, the reduction axis of the GEMM that
+ * consumes the tensor (y @ W^T), which is the operand layout of block-scaled
+ * FP8 tensor-core GEMMs.  Scales are stored row-major, [T, N / 32]; a GEMM
+ * library that wants another arrangement of the scale bytes needs a permutation.
+ * The quantised value is computed in float32 from the unrounded result.
+ */
+
+/*
+ * gbln_rmsnorm_fwd with y also (or only) delivered as MXFP8:
+ * y_e4m3 [T, H] bytes and y_scale [T, H / 32] bytes, both written.  y [T, H] io
+ * may be NULL (then only the MXFP8 copy is written).  H must be a multiple of
+ * 32.  Other arguments, aliasing and errors as gbln_rmsnorm_fwd; INVALID_ARG
+ * also for H % 32 != 0 or a null y_e4m3 / y_scale.  Any alignment is accepted.
+ */
+gbln_status gbln_rmsnorm_fwd_mxfp8(const void* x, const void* residual, const void* weight,
+                                   void* y, uint8_t* y_e4m3, uint8_t* y_scale,
+                                   void* residual_out, float* rstd, int64_t T, int64_t H,
+                                   float eps, gbln_dtype io, gbln_dtype wt,
+                                   gbln_stream_t stream);
+
+/*
+ * Gated unit forward delivered as MXFP8 only: out = f(gate) * up (as
+ * gbln_glu_fwd, with row strides ld_gate, ld_up >= I for packed [T, 2I] inputs)
+ * written as out_e4m3 [T, I] bytes (contiguous) and out_scale [T, I / 32] bytes.
+ * I must be a multiple of 32.  Errors as gbln_glu_fwd; INVALID_ARG also for
+ * I % 32 != 0.  Any alignment is accepted.
+ */
+gbln_status gbln_glu_fwd_mxfp8(const void* gate, const void* up, uint8_t* out_e4m3,
+                               uint8_t* out_scale, int64_t T, int64_t I, int64_t ld_gate,
+                               int64_t ld_up, gbln_act act, gbln_dtype io,
+                               gbln_stream_t stream);
 
 #ifdef __cplusplus
 }

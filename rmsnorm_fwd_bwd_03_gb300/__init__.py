@@ -65,6 +65,8 @@ _SIGNATURES = {
     "gbln_glu_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
     "gbln_act_fwd": (ctypes.c_int, [_vp, _vp, _i64, ctypes.c_int, ctypes.c_int, _vp]),
     "gbln_act_bwd": (ctypes.c_int, [_vp, _vp, _vp, _i64, ctypes.c_int, ctypes.c_int, _vp]),
+    "gbln_rmsnorm_fwd_mxfp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, ctypes.c_int, ctypes.c_int, _vp]),
+    "gbln_glu_fwd_mxfp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
 }
 
 _lib = None
@@ -169,6 +171,29 @@ def rmsnorm_fwd(x, weight, eps, residual=None, *, y=None, residual_out=None, rst
         T, H, float(eps), _io(x), _io(weight), _stream(x))
     _check("gbln_rmsnorm_fwd", st)
     return y, (residual_out if residual is not None else x), rstd
+
+
+def rmsnorm_fwd_mxfp8(x, weight, eps, residual=None, *, want_y=True, residual_out=None):
+    """``gbln_rmsnorm_fwd_mxfp8``.  Returns ``(y, y_e4m3, y_scale, h, rstd)``.
+
+    y_e4m3: uint8 [T, H] E4M3 codes; y_scale: uint8 [T, H / 32] E8M0 scales (one
+    per 32 consecutive values of a row); y (x's dtype) is None unless ``want_y``.
+    """
+    H = x.shape[-1]
+    T = x.numel() // H if H else 0
+    y = torch.empty_like(x) if want_y else None
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    sc = torch.empty(x.shape[:-1] + (H // 32,), dtype=torch.uint8, device=x.device)
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(x)
+    rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    st = library().gbln_rmsnorm_fwd_mxfp8(
+        _dev(x, "x"), _opt(residual, "residual"), _dev(weight, "weight"), _opt(y, "y"),
+        _dev(q, "y_e4m3"), _dev(sc, "y_scale"),
+        _opt(residual_out, "residual_out") if residual is not None else None, _dev(rstd, "rstd"),
+        T, H, float(eps), _io(x), _io(weight), _stream(x))
+    _check("gbln_rmsnorm_fwd_mxfp8", st)
+    return y, q, sc, (residual_out if residual is not None else x), rstd
 
 
 def rmsnorm_bwd_num_partials(T: int, H: int, dtype=torch.bfloat16) -> int:
@@ -458,6 +483,22 @@ def glu_fwd(gate, up, act="silu", out=None):
                                 ACT[act], _io(gate), _stream(gate))
     _check("gbln_glu_fwd", st)
     return out
+
+
+def glu_fwd_mxfp8(gate, up, act="silu"):
+    """``gbln_glu_fwd_mxfp8``: f(gate) * up delivered as MXFP8.  Returns
+    ``(out_e4m3, out_scale)``: uint8 [T, I] codes and uint8 [T, I / 32] scales.
+    gate and up may be strided row views (e.g. halves of a packed [T, 2I] tensor)."""
+    T, I, ldg = _rows2d(gate, "gate")
+    _, _, ldu = _rows2d(up, "up")
+    if up.shape != gate.shape or up.dtype != gate.dtype:
+        raise ValueError("gate and up must have the same shape and dtype")
+    q = torch.empty((T, I), dtype=torch.uint8, device=gate.device)
+    sc = torch.empty((T, I // 32), dtype=torch.uint8, device=gate.device)
+    st = library().gbln_glu_fwd_mxfp8(gate.data_ptr(), up.data_ptr(), q.data_ptr(), sc.data_ptr(),
+                                      T, I, ldg, ldu, ACT[act], _io(gate), _stream(gate))
+    _check("gbln_glu_fwd_mxfp8", st)
+    return q, sc
 
 
 def glu_bwd(dout, gate, up, act="silu", dgate=None, dup=None):

@@ -5,6 +5,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "gbln.h"
@@ -155,6 +156,69 @@ __device__ __forceinline__ void load_weight(const W* w, int iv, float (&out)[VEC
 // Sum of v over the TPR threads of a row group; identical value in every thread.
 // TPR <= 32: shuffles.  TPR > 32 (one row per block): shuffles + shared memory
 // red[TPR / 32]; safe to call back to back.
+// ---------------------------------------------------------------------------
+// MXFP8 output (OCP Microscaling Formats (MX) v1.0): E4M3 elements, and one
+// E8M0 scale byte (exponent + 127) per block of 32 consecutive values of a row.
+// The shared exponent is floor(log2(amax)) - 8, 8 being the exponent of E4M3's
+// largest normal (1.75 * 2^8), clamped to E8M0's [-127, 127]; an all-zero
+// block takes -127.  Elements are value / 2^exponent rounded to nearest even
+// and saturated to +-448 by the hardware conversion.
+// ---------------------------------------------------------------------------
+constexpr int kMxBlock = 32;
+
+__device__ __forceinline__ int mx_shared_exp(float amax) {
+  const int eb = (int)((__float_as_uint(amax) >> 23) & 0xffu);  // 0 for zero and subnormals
+  const int se = eb - 127 - 8;
+  return eb == 0 ? -127 : (se < -127 ? -127 : se);
+}
+// 2^-se, exact (se in [-127, 119] gives a normal float).
+__device__ __forceinline__ float mx_inv_scale(int se) {
+  return __uint_as_float((uint32_t)(127 - se) << 23);
+}
+// Two E4M3 codes, a in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Quantise this lane's VEC consecutive values o of an MX block that spans
+// 32 / VEC consecutive lanes (aligned to 32 / VEC within the warp).  All 32
+// lanes of the warp must call it; lanes with active == false contribute
+// nothing and store nothing.  q: this lane's first code; sc: the block's scale
+// byte, written by the block's first lane (first == true).
+template <int VEC>
+__device__ __forceinline__ void mx_store(const float (&o)[VEC], bool active, bool first,
+                                         uint8_t* q, uint8_t* sc) {
+  constexpr int LB = kMxBlock / VEC;
+  float a = 0.f;
+  if (active) {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) a = fmaxf(a, fabsf(o[e]));
+  }
+#pragma unroll
+  for (int m = 1; m < LB; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+  if (!active) return;
+  const int se = mx_shared_exp(a);
+  const float inv = mx_inv_scale(se);
+  if constexpr (VEC == 8) {
+    uint2 p;
+    p.x = e4m3x2(o[0] * inv, o[1] * inv) | (e4m3x2(o[2] * inv, o[3] * inv) << 16);
+    p.y = e4m3x2(o[4] * inv, o[5] * inv) | (e4m3x2(o[6] * inv, o[7] * inv) << 16);
+    *reinterpret_cast<uint2*>(q) = p;
+  } else if constexpr (VEC == 4) {
+    *reinterpret_cast<uint32_t*>(q) =
+        e4m3x2(o[0] * inv, o[1] * inv) | (e4m3x2(o[2] * inv, o[3] * inv) << 16);
+  } else {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) q[e] = (uint8_t)(e4m3x2(o[e] * inv, 0.f) & 0xffu);
+  }
+  if (first) *sc = (uint8_t)(se + 127);
+}
+
+struct MxOut {
+  uint8_t* q;   // [rows, H] E4M3 codes
+  uint8_t* sc;  // [rows, H / 32] E8M0 scales
+};
+
 template <int TPR>
 __device__ __forceinline__ float row_sum(float v, float* red) {
   if constexpr (TPR <= 32) {

@@ -300,6 +300,51 @@ act_bwd_kernel(const T* dy, const T* x, T* dx, int64_t nv) {
 }
 
 // ---------------------------------------------------------------------------
+// Forward with MXFP8 output (codes [T, I] and one scale byte per 32 values of
+// a row), for the down projection's FP8 operand.  Same units as glu_fwd_rows;
+// I is a multiple of 32, so an MX block is 32 / VEC consecutive column
+// vectors, held by consecutive lanes.  Every lane runs the quantisation (its
+// warp shuffles need all 32), inactive lanes with nothing to store.
+// ---------------------------------------------------------------------------
+template <typename T, int VEC, int ACT, int UNROLL>
+__global__ void __launch_bounds__(kGluBlock)
+glu_fwd_mx(const T* gate, const T* up, MxOut mx, int64_t T_, int64_t ncol, int64_t ldg,
+           int64_t ldu) {
+  constexpr int LB = kMxBlock / VEC;
+  const int64_t I = ncol * VEC;
+  const int64_t ncb = (ncol + kGluBlock - 1) / kGluBlock;
+  const int64_t units = (T_ + UNROLL - 1) / UNROLL * ncb;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int64_t rg = u / ncb;
+    const int64_t c = (u - rg * ncb) * kGluBlock + threadIdx.x;
+    const bool colok = c < ncol;
+    const int64_t r0 = rg * UNROLL;
+    Packed<T, VEC> g[UNROLL], v[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      if (colok && r0 + k < T_) {
+        g[k].load(gate + (r0 + k) * ldg + c * VEC);
+        v[k].load(up + (r0 + k) * ldu + c * VEC);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      if (r0 + k >= T_) break;  // uniform across the block
+      float o[VEC];
+      if (colok) {
+        float gf[VEC], uf[VEC];
+        g[k].get(gf);
+        v[k].get(uf);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] = act_f<T, ACT>(gf[e]) * uf[e];
+      }
+      mx_store<VEC>(o, colok, c % LB == 0, mx.q + (r0 + k) * I + c * VEC,
+                    mx.sc + (r0 + k) * (I / kMxBlock) + c / LB);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
@@ -331,6 +376,25 @@ void glu_fwd_launch(const void* g, const void* u, void* o, int64_t rows, int64_t
     const int64_t units = (rows + U - 1) / U * ((I + kGluBlock - 1) / kGluBlock);
     glu_fwd_rows<T, 1, ACT, U><<<resident_grid(units), kGluBlock, 0, s>>>(
         (const T*)g, (const T*)u, (T*)o, rows, I, ldg, ldu, ldo);
+  }
+}
+
+template <typename T, int ACT>
+void glu_fwd_mx_launch(const void* g, const void* u, MxOut mx, int64_t rows, int64_t I, int64_t ldg,
+                       int64_t ldu, cudaStream_t s) {
+  constexpr int VEC = VecOf<T>::N;
+  constexpr int U = 4;
+  const bool vec = aligned16(g) && aligned16(u) && ldg % VEC == 0 && ldu % VEC == 0 &&
+                   reinterpret_cast<uintptr_t>(mx.q) % VEC == 0;  // VEC codes per lane
+  if (vec) {
+    const int64_t ncol = I / VEC;
+    const int64_t units = (rows + U - 1) / U * ((ncol + kGluBlock - 1) / kGluBlock);
+    glu_fwd_mx<T, VEC, ACT, U><<<resident_grid(units), kGluBlock, 0, s>>>((const T*)g, (const T*)u, mx,
+                                                                          rows, ncol, ldg, ldu);
+  } else {
+    const int64_t units = (rows + U - 1) / U * ((I + kGluBlock - 1) / kGluBlock);
+    glu_fwd_mx<T, 1, ACT, U><<<resident_grid(units), kGluBlock, 0, s>>>((const T*)g, (const T*)u, mx,
+                                                                        rows, I, ldg, ldu);
   }
 }
 
@@ -432,6 +496,27 @@ extern "C" gbln_status gbln_glu_fwd(const void* gate, const void* up, void* out,
     GBLN_DISPATCH_ACT(bf16, act, GBLN_GLU_FWD)
   }
 #undef GBLN_GLU_FWD
+  return launch_status();
+}
+
+extern "C" gbln_status gbln_glu_fwd_mxfp8(const void* gate, const void* up, uint8_t* out_e4m3,
+                                          uint8_t* out_scale, int64_t T, int64_t I,
+                                          int64_t ld_gate, int64_t ld_up, gbln_act act,
+                                          gbln_dtype io, gbln_stream_t stream) {
+  if (!dtype_ok(io) || !act_ok(act) || !sizes_ok(T, I) || I % kMxBlock != 0) return GBLN_ERR_INVALID_ARG;
+  if (!ld_ok(T, I, ld_gate) || !ld_ok(T, I, ld_up)) return GBLN_ERR_INVALID_ARG;
+  if (T == 0) return GBLN_OK;  // nothing is read or written: pointers are not examined
+  if (!gate || !up || !out_e4m3 || !out_scale) return GBLN_ERR_INVALID_ARG;
+  if (sm_count() <= 0) return GBLN_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  const MxOut mx{out_e4m3, out_scale};
+#define GBLN_GLU_FWD_MX(TY, A) glu_fwd_mx_launch<TY, A>(gate, up, mx, T, I, ld_gate, ld_up, s)
+  if (io == GBLN_F32) {
+    GBLN_DISPATCH_ACT(float, act, GBLN_GLU_FWD_MX)
+  } else {
+    GBLN_DISPATCH_ACT(bf16, act, GBLN_GLU_FWD_MX)
+  }
+#undef GBLN_GLU_FWD_MX
   return launch_status();
 }
 

@@ -29,10 +29,11 @@ constexpr int kGenericBlock = 256;
 // Forward, vector path.  A row group of TPR threads owns one row; thread l owns
 // the 16-byte vectors l, l + TPR, ..., (VPT of them).  BLOCK / TPR rows per block.
 // ---------------------------------------------------------------------------
-template <typename T, typename W, int TPR, int VPT, int BLOCK, bool RES>
+// MX: y is also written as MXFP8 (mx.q, mx.sc); y itself may then be null.
+template <typename T, typename W, int TPR, int VPT, int BLOCK, bool RES, bool MX = false>
 __global__ void __launch_bounds__(BLOCK)
 rms_fwd_vec(const T* x, const T* r, const W* __restrict__ w, T* y, T* hout,
-            float* __restrict__ rstd, int64_t rows, int H, float inv_H, float eps) {
+            float* __restrict__ rstd, int64_t rows, int H, float inv_H, float eps, MxOut mx = {}) {
   constexpr int VEC = VecOf<T>::N;
   constexpr int RPC = BLOCK / TPR;
   __shared__ float red[BLOCK / 32 > 0 ? BLOCK / 32 : 1];
@@ -76,12 +77,19 @@ rms_fwd_vec(const T* x, const T* r, const W* __restrict__ w, T* y, T* hout,
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int iv = l + v * TPR;
+    float o[VEC];
     if (iv < nvec) {
-      float wv[VEC], o[VEC];
+      float wv[VEC];
       load_weight<W, VEC>(w, iv, wv);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) o[e] = wv[e] * (h[v][e] * rs);
-      st_vec(y + base + (size_t)iv * VEC, pack<T, VEC>(o));
+      if (!MX || y) st_vec(y + base + (size_t)iv * VEC, pack<T, VEC>(o));
+    }
+    if constexpr (MX) {
+      // an MX block is 32 / VEC consecutive vectors: lanes l .. l + 32 / VEC - 1
+      constexpr int LB = kMxBlock / VEC;
+      mx_store<VEC>(o, iv < nvec, iv % LB == 0, mx.q + base + (size_t)iv * VEC,
+                    mx.sc + (size_t)row * (H / kMxBlock) + iv / LB);
     }
   }
 }
@@ -90,10 +98,10 @@ rms_fwd_vec(const T* x, const T* r, const W* __restrict__ w, T* y, T* hout,
 // Forward, element-wise path (any alignment, any H): one block per row, two
 // passes over the row; the second re-reads h (cache hit for all but huge H).
 // ---------------------------------------------------------------------------
-template <typename T, typename W, bool RES>
+template <typename T, typename W, bool RES, bool MX = false>
 __global__ void __launch_bounds__(kGenericBlock)
 rms_fwd_generic(const T* x, const T* r, const W* __restrict__ w, T* y, T* hout,
-                float* __restrict__ rstd, int64_t rows, int H, float inv_H, float eps) {
+                float* __restrict__ rstd, int64_t rows, int H, float inv_H, float eps, MxOut mx = {}) {
   __shared__ float red[kGenericBlock / 32];
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
     const size_t base = (size_t)row * H;
@@ -110,9 +118,13 @@ rms_fwd_generic(const T* x, const T* r, const W* __restrict__ w, T* y, T* hout,
     ss = row_sum<kGenericBlock>(ss, red);
     const float rs = rsqrtf(ss * inv_H + eps);
     if (threadIdx.x == 0) rstd[row] = rs;
+    // With MX, H is a multiple of 32, so each warp's pass covers one MX block.
     for (int j = threadIdx.x; j < H; j += kGenericBlock) {
       const float a = RES ? to_f32(hout[base + j]) : to_f32(x[base + j]);  // own write
-      y[base + j] = from_f32<T>(to_f32(w[j]) * (a * rs));
+      float o[1] = {to_f32(w[j]) * (a * rs)};
+      if (!MX || y) y[base + j] = from_f32<T>(o[0]);
+      if constexpr (MX)
+        mx_store<1>(o, true, j % kMxBlock == 0, mx.q + base + j, mx.sc + (size_t)row * (H / kMxBlock) + j / kMxBlock);
     }
   }
 }
@@ -309,47 +321,50 @@ int64_t partials_for(int64_t T, const Geometry& g, int sms) {
   return P < 1 ? 1 : P;
 }
 
-template <typename T, typename W, int TPR, int VPT, int BLOCK>
+template <typename T, typename W, int TPR, int VPT, int BLOCK, bool MX>
 void fwd_vec(bool res, const void* x, const void* r, const void* w, void* y, void* hout,
-             float* rstd, int64_t rows, int H, float inv_H, float eps, cudaStream_t s) {
+             float* rstd, int64_t rows, int H, float inv_H, float eps, MxOut mx, cudaStream_t s) {
   const unsigned grid = (unsigned)((rows + BLOCK / TPR - 1) / (BLOCK / TPR));
   if (res)
-    rms_fwd_vec<T, W, TPR, VPT, BLOCK, true><<<grid, BLOCK, 0, s>>>(
-        (const T*)x, (const T*)r, (const W*)w, (T*)y, (T*)hout, rstd, rows, H, inv_H, eps);
+    rms_fwd_vec<T, W, TPR, VPT, BLOCK, true, MX><<<grid, BLOCK, 0, s>>>(
+        (const T*)x, (const T*)r, (const W*)w, (T*)y, (T*)hout, rstd, rows, H, inv_H, eps, mx);
   else
-    rms_fwd_vec<T, W, TPR, VPT, BLOCK, false><<<grid, BLOCK, 0, s>>>(
-        (const T*)x, nullptr, (const W*)w, (T*)y, nullptr, rstd, rows, H, inv_H, eps);
+    rms_fwd_vec<T, W, TPR, VPT, BLOCK, false, MX><<<grid, BLOCK, 0, s>>>(
+        (const T*)x, nullptr, (const W*)w, (T*)y, nullptr, rstd, rows, H, inv_H, eps, mx);
 }
 
-template <typename T, typename W>
+template <typename T, typename W, bool MX = false>
 gbln_status fwd_typed(const void* x, const void* r, const void* w, void* y, void* hout,
-                      float* rstd, int64_t rows, int64_t H, float eps, cudaStream_t s) {
+                      float* rstd, int64_t rows, int64_t H, float eps, cudaStream_t s,
+                      MxOut mx = {}) {
   const bool res = r != nullptr;
   const Geometry g = geometry(H, sizeof(T));
+  constexpr size_t kCodeAlign = 16 / sizeof(T);  // bytes of codes per 16-byte input vector
   const bool vec = g.vec && aligned16(x) && aligned16(w) && aligned16(y) &&
-                   (!res || (aligned16(r) && aligned16(hout)));
+                   (!res || (aligned16(r) && aligned16(hout))) &&
+                   (!MX || (reinterpret_cast<uintptr_t>(mx.q) % kCodeAlign) == 0);
   const float inv_H = 1.0f / (float)H;
   const int h = (int)H;
   if (!vec) {
     const unsigned grid = (unsigned)(rows < 65535LL * 32 ? rows : 65535LL * 32);
     if (res)
-      rms_fwd_generic<T, W, true><<<grid, kGenericBlock, 0, s>>>(
-          (const T*)x, (const T*)r, (const W*)w, (T*)y, (T*)hout, rstd, rows, h, inv_H, eps);
+      rms_fwd_generic<T, W, true, MX><<<grid, kGenericBlock, 0, s>>>(
+          (const T*)x, (const T*)r, (const W*)w, (T*)y, (T*)hout, rstd, rows, h, inv_H, eps, mx);
     else
-      rms_fwd_generic<T, W, false><<<grid, kGenericBlock, 0, s>>>(
-          (const T*)x, nullptr, (const W*)w, (T*)y, nullptr, rstd, rows, h, inv_H, eps);
+      rms_fwd_generic<T, W, false, MX><<<grid, kGenericBlock, 0, s>>>(
+          (const T*)x, nullptr, (const W*)w, (T*)y, nullptr, rstd, rows, h, inv_H, eps, mx);
     return launch_status();
   }
   if (g.tpr == 32) {
-    if (g.vpt == 1) fwd_vec<T, W, 32, 1, kWarpBlock>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, s);
-    else if (g.vpt == 2) fwd_vec<T, W, 32, 2, kWarpBlock>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, s);
-    else fwd_vec<T, W, 32, 4, kWarpBlock>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, s);
+    if (g.vpt == 1) fwd_vec<T, W, 32, 1, kWarpBlock, MX>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, mx, s);
+    else if (g.vpt == 2) fwd_vec<T, W, 32, 2, kWarpBlock, MX>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, mx, s);
+    else fwd_vec<T, W, 32, 4, kWarpBlock, MX>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, mx, s);
   } else {
     switch (g.tpr) {
-      case 64: fwd_vec<T, W, 64, 4, 64>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, s); break;
-      case 128: fwd_vec<T, W, 128, 4, 128>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, s); break;
-      case 256: fwd_vec<T, W, 256, 4, 256>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, s); break;
-      default: fwd_vec<T, W, 512, 4, 512>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, s); break;
+      case 64: fwd_vec<T, W, 64, 4, 64, MX>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, mx, s); break;
+      case 128: fwd_vec<T, W, 128, 4, 128, MX>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, mx, s); break;
+      case 256: fwd_vec<T, W, 256, 4, 256, MX>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, mx, s); break;
+      default: fwd_vec<T, W, 512, 4, 512, MX>(res, x, r, w, y, hout, rstd, rows, h, inv_H, eps, mx, s); break;
     }
   }
   return launch_status();
@@ -432,6 +447,27 @@ extern "C" gbln_status gbln_rmsnorm_fwd(const void* x, const void* residual, con
   if (io == GBLN_F32) return fwd_typed<float, float>(x, r, weight, y, ho, rstd, T, H, eps, s);
   if (wt == GBLN_BF16) return fwd_typed<bf16, bf16>(x, r, weight, y, ho, rstd, T, H, eps, s);
   return fwd_typed<bf16, float>(x, r, weight, y, ho, rstd, T, H, eps, s);
+}
+
+extern "C" gbln_status gbln_rmsnorm_fwd_mxfp8(const void* x, const void* residual,
+                                              const void* weight, void* y, uint8_t* y_e4m3,
+                                              uint8_t* y_scale, void* residual_out, float* rstd,
+                                              int64_t T, int64_t H, float eps, gbln_dtype io,
+                                              gbln_dtype wt, gbln_stream_t stream) {
+  if (!dtype_ok(io) || !dtype_ok(wt)) return GBLN_ERR_INVALID_ARG;
+  if (T < 0 || T > kMaxRows || H <= 0 || H > kMaxH || H % kMxBlock != 0) return GBLN_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f && eps <= 3.4028235e38f)) return GBLN_ERR_INVALID_ARG;
+  if (!dtypes_ok(io, wt)) return GBLN_ERR_UNSUPPORTED;
+  if (T == 0) return GBLN_OK;  // nothing is read or written: pointers are not examined
+  if (!x || !weight || !y_e4m3 || !y_scale || !rstd) return GBLN_ERR_INVALID_ARG;
+  if (residual && !residual_out) return GBLN_ERR_INVALID_ARG;
+  const void* r = residual;
+  void* ho = residual ? residual_out : nullptr;
+  const MxOut mx{y_e4m3, y_scale};
+  cudaStream_t s = (cudaStream_t)stream;
+  if (io == GBLN_F32) return fwd_typed<float, float, true>(x, r, weight, y, ho, rstd, T, H, eps, s, mx);
+  if (wt == GBLN_BF16) return fwd_typed<bf16, bf16, true>(x, r, weight, y, ho, rstd, T, H, eps, s, mx);
+  return fwd_typed<bf16, float, true>(x, r, weight, y, ho, rstd, T, H, eps, s, mx);
 }
 
 extern "C" int64_t gbln_rmsnorm_bwd_num_partials(int64_t T, int64_t H, gbln_dtype io) {

@@ -107,3 +107,44 @@ class Guarded:
         head = b[: self.band * esz]
         tail = b[(self.band + self.n) * esz:]
         return bool((head == self.fill).all()) and bool((tail == self.fill).all())
+
+
+# MXFP8 codes are integers decided by floating point.  The kernel decides them
+# from its float32 result, the oracle from the exact one; the two differ by at
+# most the float32 bound above: relative 1e-5 (plus, where an activation
+# cancels, an absolute term relative to the block's largest magnitude:
+# ``abs_rel``).
+# Wherever moving the exact value by that much cannot change a decision, the
+# code (and the scale) must be identical; where it can, the kernel's must lie
+# between the two outcomes.
+MX_REL = 1e-5
+
+
+def check_mxfp8(q_gpu, sc_gpu, v64, what: str, rel: float = MX_REL, abs_rel: float = 0.0,
+                max_ambiguous: float = 1e-3):
+    import oracle
+    q = q_gpu.cpu().numpy()
+    sc = sc_gpu.cpu().numpy()
+    v = np.asarray(v64, dtype=np.float64)
+    T, N = v.shape
+    assert q.shape == (T, N) and sc.shape == (T, N // 32), (what, q.shape, sc.shape)
+    vb = v.reshape(T, N // 32, 32)
+    amax = np.abs(vb).max(axis=-1)
+    se_lo = oracle.mx_scale_exponent(amax * (1 - rel))
+    se_hi = oracle.mx_scale_exponent(amax * (1 + rel))
+    se = sc.astype(np.int64) - 127
+    bad = (se != se_lo) & (se != se_hi)
+    assert not bad.any(), f"{what}: {bad.sum()} scale bytes off, first at {np.argwhere(bad)[0]}"
+    t = vb / np.ldexp(1.0, se)[..., None]                     # exact values in the kernel's scale
+    win = rel * np.abs(t) + abs_rel * (amax / np.ldexp(1.0, se))[..., None]
+    lo = oracle.round_to_e4m3(t - win)                         # rounding is monotone
+    hi = oracle.round_to_e4m3(t + win)
+    got = oracle.e4m3_decode(q.reshape(T, N // 32, 32))
+    bad = ~((got >= lo) & (got <= hi))
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {bad.sum()} codes off; first at {i}: gpu {got[i]!r}, "
+                             f"exact {t[i]!r} -> [{lo[i]!r}, {hi[i]!r}]")
+    amb = int((lo != hi).sum())
+    if lo.size >= 4096:  # too few codes say nothing about the rate
+        assert amb <= max_ambiguous * lo.size, f"{what}: {amb} of {lo.size} codes sit on a decision boundary"

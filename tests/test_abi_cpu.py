@@ -191,6 +191,26 @@ def test_glu_and_act_reject(lib):
     assert lib.gbln_act_bwd(None, None, None, 0, 1, BF16, None) == OK
 
 
+def test_mxfp8_entries_reject(lib):
+    f = FAKE
+    # H / I not a multiple of the 32-value MX block
+    assert lib.gbln_rmsnorm_fwd_mxfp8(f, None, f, None, f, f, None, f, 4, 48, 1e-6, BF16, BF16, None) == INVALID
+    assert lib.gbln_glu_fwd_mxfp8(f, f, f, f, 4, 48, 48, 48, 0, BF16, None) == INVALID
+    # null code / scale outputs; null x; residual without residual_out
+    assert lib.gbln_rmsnorm_fwd_mxfp8(f, None, f, None, None, f, None, f, 4, 64, 1e-6, BF16, BF16, None) == INVALID
+    assert lib.gbln_rmsnorm_fwd_mxfp8(f, None, f, None, f, None, None, f, 4, 64, 1e-6, BF16, BF16, None) == INVALID
+    assert lib.gbln_rmsnorm_fwd_mxfp8(None, None, f, None, f, f, None, f, 4, 64, 1e-6, BF16, BF16, None) == INVALID
+    assert lib.gbln_rmsnorm_fwd_mxfp8(f, f, f, None, f, f, None, f, 4, 64, 1e-6, BF16, BF16, None) == INVALID
+    assert lib.gbln_rmsnorm_fwd_mxfp8(f, None, f, None, f, f, None, f, 4, 64, -1.0, BF16, BF16, None) == INVALID
+    assert lib.gbln_rmsnorm_fwd_mxfp8(f, None, f, None, f, f, None, f, 4, 64, 1e-6, F32, BF16, None) == UNSUPPORTED
+    assert lib.gbln_glu_fwd_mxfp8(f, f, None, f, 4, 64, 64, 64, 0, BF16, None) == INVALID
+    assert lib.gbln_glu_fwd_mxfp8(f, f, f, f, 4, 64, 63, 64, 0, BF16, None) == INVALID  # ld < I
+    assert lib.gbln_glu_fwd_mxfp8(f, f, f, f, 4, 64, 64, 64, 9, BF16, None) == INVALID  # bad act
+    # T == 0 is a no-op before any pointer is examined
+    assert lib.gbln_rmsnorm_fwd_mxfp8(None, None, None, None, None, None, None, None, 0, 64, 1e-6, BF16, BF16, None) == OK
+    assert lib.gbln_glu_fwd_mxfp8(None, None, None, None, 0, 64, 64, 64, 0, BF16, None) == OK
+
+
 def test_device_error_rejects_null(lib):
     assert lib.gbln_device_error(None, 0) == INVALID
 
