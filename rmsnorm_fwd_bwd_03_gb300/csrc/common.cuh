@@ -219,6 +219,11 @@ struct MxOut {
   uint8_t* sc;  // [rows, H / 32] E8M0 scales
 };
 
+// Barrier `id` (1..15) over `threads` threads of the block (a multiple of 32).
+__device__ __forceinline__ void bar_sync_named(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 template <int TPR>
 __device__ __forceinline__ float row_sum(float v, float* red) {
   if constexpr (TPR <= 32) {
@@ -236,8 +241,9 @@ __device__ __forceinline__ float row_sum(float v, float* red) {
   }
 }
 
-// Fixed-order column sums of a [P, ld] float32 buffer: out[j] = (acc ? out[j] :
-// 0) + sum_p partial[p * ld + j] for j < ncol.  Block (32, kColSumStripes):
+// Fixed-order column sums of a [P, ld] float32 buffer: o[j] = (acc ? o[j] : 0)
+// + sum_p partial[p * ld + j] for j < ncol, where o is out0 for j < split and
+// out1 - split beyond (dW and dB of one [P, 2H] buffer in one launch).  Block (32, kColSumStripes):
 // column j = 32 * blockIdx.x + tx; row stripe ty sums p = ty, ty + stripes, ...
 // in order (loads unrolled so several are in flight; the additions stay in
 // that order), then the stripes are added in order.  Bitwise reproducible.
@@ -245,8 +251,8 @@ constexpr int kColSumStripes = 32;
 
 template <int DUMMY = 0>
 __global__ void __launch_bounds__(32 * kColSumStripes)
-colsum_kernel(const float* __restrict__ partial, int64_t P, int ncol, int ld, float* out,
-              int accumulate) {
+colsum_kernel(const float* __restrict__ partial, int64_t P, int ncol, int ld, float* out0,
+              float* out1, int split, int accumulate) {
   __shared__ float s[kColSumStripes][33];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int j = blockIdx.x * 32 + tx;
@@ -261,7 +267,8 @@ colsum_kernel(const float* __restrict__ partial, int64_t P, int ncol, int ld, fl
     float t = 0.f;
 #pragma unroll
     for (int q = 0; q < kColSumStripes; ++q) t += s[q][tx];
-    out[j] = accumulate ? out[j] + t : t;
+    float* o = j < split ? out0 + j : out1 + (j - split);
+    *o = accumulate ? *o + t : t;
   }
 }
 

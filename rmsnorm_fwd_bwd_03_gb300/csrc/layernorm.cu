@@ -265,24 +265,27 @@ ln_bwd_vec(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
 }
 
 // Backward, vector path for one row per block (TPR = BLOCK > 32): the dW and
-// dB accumulators live in shared memory, slot k of thread t at acc[k * TPR + t]
-// (consecutive threads hit consecutive banks), instead of in registers, so the
-// kernel fits 64 registers and 1024 threads stay resident per SM.
+// dB accumulators live in shared memory instead of registers, so the kernel
+// fits 64 registers and 1024 threads stay resident per SM.  Four consecutive
+// columns of a thread form one 16-byte slot, slot k of thread t at acc[k * TPR
+// + t] (consecutive threads hit consecutive 16-byte bank groups), so each
+// read-modify-write covers four columns.
 template <typename T, typename W, int TPR, int VPT, bool DRES>
 __global__ void __launch_bounds__(TPR, 1024 / TPR)
 ln_bwd_cta(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
            const float* __restrict__ mean, const float* __restrict__ rstd, T* dx,
            float* __restrict__ partial, int64_t rows, int H, float inv_H) {
   constexpr int VEC = VecOf<T>::N;
-  constexpr int NACC = VPT * VEC;  // accumulator slots per thread and gradient
-  extern __shared__ float acc[];   // [2 * NACC][TPR]: dW slots, then dB slots
+  constexpr int Q = VEC / 4;         // 16-byte slots per vector
+  constexpr int NSL = VPT * Q;       // slots per thread and gradient
+  extern __shared__ float4 acc[];    // [2 * NSL][TPR]: dW slots, then dB slots
   __shared__ float red[TPR / 32];
   const int l = threadIdx.x;
   const int nvec = H / VEC;
   const int64_t P = gridDim.x, p = blockIdx.x;
   const int64_t r0 = p * rows / P, r1 = (p + 1) * rows / P;
 #pragma unroll
-  for (int k = 0; k < 2 * NACC; ++k) acc[k * TPR + l] = 0.f;
+  for (int k = 0; k < 2 * NSL; ++k) acc[k * TPR + l] = make_float4(0.f, 0.f, 0.f, 0.f);
 
   for (int64_t row = r0; row < r1; ++row) {  // same trip count in every thread
     const size_t base = (size_t)row * H;
@@ -312,10 +315,19 @@ ln_bwd_cta(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
           const float gg = d[e] * wv[e];
           sg += gg;
           sgn = fmaf(gg, n[e], sgn);
-          float* aw = acc + (v * VEC + e) * TPR + l;
-          float* ab = acc + (NACC + v * VEC + e) * TPR + l;
-          *aw = fmaf(d[e], n[e], *aw);
-          *ab += d[e];
+        }
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+          float4* aw = acc + (v * Q + q) * TPR + l;
+          float4* ab = acc + (NSL + v * Q + q) * TPR + l;
+          float4 a = *aw, b = *ab;
+          a.x = fmaf(d[4 * q], n[4 * q], a.x);
+          a.y = fmaf(d[4 * q + 1], n[4 * q + 1], a.y);
+          a.z = fmaf(d[4 * q + 2], n[4 * q + 2], a.z);
+          a.w = fmaf(d[4 * q + 3], n[4 * q + 3], a.w);
+          b.x += d[4 * q]; b.y += d[4 * q + 1]; b.z += d[4 * q + 2]; b.w += d[4 * q + 3];
+          *aw = a;
+          *ab = b;
         }
       }
     }
@@ -347,11 +359,141 @@ ln_bwd_cta(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
     const int iv = l + v * TPR;
     if (iv < nvec) {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        prow[iv * VEC + e] = acc[(v * VEC + e) * TPR + l];
-        prow[H + iv * VEC + e] = acc[(NACC + v * VEC + e) * TPR + l];
+      for (int q = 0; q < Q; ++q) {
+        *reinterpret_cast<float4*>(prow + iv * VEC + 4 * q) = acc[(v * Q + q) * TPR + l];
+        *reinterpret_cast<float4*>(prow + H + iv * VEC + 4 * q) = acc[(NSL + v * Q + q) * TPR + l];
       }
     }
+  }
+}
+
+// Backward for rows of 65..128 vectors: kLnGroups row groups of 64 threads per
+// block, each with its own shared-memory accumulators (layout as ln_bwd_cta) and
+// its own named barrier for the row sums, so groups walk their rows (r0 + g,
+// r0 + g + kLnGroups, ...) independently.  At 64 registers 1024 threads stay
+// resident per SM while the block count, and with it the number of partial
+// rows, stays at 4 per SM.  The groups' accumulators are summed in a fixed
+// order at the end.
+constexpr int kLnGroups = 4;
+constexpr int kLnGroupThreads = 64;
+
+template <typename T, typename W, int VPT, bool DRES>
+__global__ void __launch_bounds__(kLnGroups * kLnGroupThreads, 1024 / (kLnGroups * kLnGroupThreads))
+ln_bwd_grp(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
+           const float* __restrict__ mean, const float* __restrict__ rstd, T* dx,
+           float* __restrict__ partial, int64_t rows, int H, float inv_H) {
+  constexpr int TPR = kLnGroupThreads;
+  constexpr int VEC = VecOf<T>::N;
+  constexpr int Q = VEC / 4;
+  constexpr int NSL = VPT * Q;
+  extern __shared__ float4 acc_all[];  // [kLnGroups][2 * NSL][TPR]
+  __shared__ float2 red2[kLnGroups][2][TPR / 32];
+  const int g = threadIdx.x / TPR, l = threadIdx.x % TPR, lane = threadIdx.x % 32;
+  float4* acc = acc_all + (size_t)g * 2 * NSL * TPR;
+  const int nvec = H / VEC;
+  const int64_t P = gridDim.x, p = blockIdx.x;
+  const int64_t r0 = p * rows / P, r1 = (p + 1) * rows / P;
+#pragma unroll
+  for (int k = 0; k < 2 * NSL; ++k) acc[k * TPR + l] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+  int par = 0;
+  for (int64_t row = r0 + g; row < r1; row += kLnGroups) {
+    const size_t base = (size_t)row * H;
+    uint4 dya[VPT], ha[VPT], dra[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int iv = l + v * TPR;
+      if (iv < nvec) {
+        dya[v] = ld_stream(dy + base + (size_t)iv * VEC);
+        ha[v] = ld_stream(h + base + (size_t)iv * VEC);
+        if constexpr (DRES) dra[v] = ld_stream(dres + base + (size_t)iv * VEC);
+      }
+    }
+    const float mu = mean[row], rs = rstd[row];
+    float sg = 0.f, sgn = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int iv = l + v * TPR;
+      if (iv < nvec) {
+        float d[VEC], n[VEC], wv[VEC];
+        unpack<VEC>(dya[v], d);
+        unpack<VEC>(ha[v], n);
+        load_weight<W, VEC>(w, iv, wv);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          n[e] = (n[e] - mu) * rs;
+          const float gg = d[e] * wv[e];
+          sg += gg;
+          sgn = fmaf(gg, n[e], sgn);
+        }
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+          float4* aw = acc + (v * Q + q) * TPR + l;
+          float4* ab = acc + (NSL + v * Q + q) * TPR + l;
+          float4 a = *aw, b = *ab;
+          a.x = fmaf(d[4 * q], n[4 * q], a.x);
+          a.y = fmaf(d[4 * q + 1], n[4 * q + 1], a.y);
+          a.z = fmaf(d[4 * q + 2], n[4 * q + 2], a.z);
+          a.w = fmaf(d[4 * q + 3], n[4 * q + 3], a.w);
+          b.x += d[4 * q]; b.y += d[4 * q + 1]; b.z += d[4 * q + 2]; b.w += d[4 * q + 3];
+          *aw = a;
+          *ab = b;
+        }
+      }
+    }
+    // Row sums over the group's two warps.  red2 is double-buffered by row
+    // parity: a thread can only write a buffer again after the group's next
+    // barrier, which every thread reaches after reading this one.
+    sg = group_sum<32>(sg);
+    sgn = group_sum<32>(sgn);
+    if (lane == 0) red2[g][par][l / 32] = make_float2(sg, sgn);
+    bar_sync_named(1 + g, TPR);
+    float2 ssum = red2[g][par][0];
+#pragma unroll
+    for (int k = 1; k < TPR / 32; ++k) {
+      ssum.x += red2[g][par][k].x;
+      ssum.y += red2[g][par][k].y;
+    }
+    par ^= 1;
+    const float mg = ssum.x * inv_H, mgn = ssum.y * inv_H;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int iv = l + v * TPR;
+      if (iv < nvec) {
+        float d[VEC], n[VEC], wv[VEC], o[VEC];
+        unpack<VEC>(dya[v], d);
+        unpack<VEC>(ha[v], n);
+        load_weight<W, VEC>(w, iv, wv);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] = rs * (d[e] * wv[e] - mg - ((n[e] - mu) * rs) * mgn);
+        if constexpr (DRES) {
+          float d2[VEC];
+          unpack<VEC>(dra[v], d2);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) o[e] += d2[e];
+        }
+        st_vec(dx + base + (size_t)iv * VEC, pack<T, VEC>(o));
+      }
+    }
+  }
+  __syncthreads();
+  // Fixed-order sum over the groups: column j is component j % 4 of slot
+  // (v * Q + (j % VEC) / 4) of thread l, where j / VEC = l + v * TPR.
+  float* prow = partial + (size_t)p * 2 * H;
+  const float* af = reinterpret_cast<const float*>(acc_all);
+  for (int j = threadIdx.x; j < H; j += kLnGroups * TPR) {
+    const int iv = j / VEC, e = j % VEC;
+    const int lt = iv % TPR, v = iv / TPR;
+    const size_t sw = ((size_t)(v * Q + e / 4) * TPR + lt) * 4 + e % 4;
+    const size_t sb = ((size_t)(NSL + v * Q + e / 4) * TPR + lt) * 4 + e % 4;
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int q = 0; q < kLnGroups; ++q) {
+      a += af[(size_t)q * 2 * NSL * TPR * 4 + sw];
+      b += af[(size_t)q * 2 * NSL * TPR * 4 + sb];
+    }
+    prow[j] = a;
+    prow[H + j] = b;
   }
 }
 
@@ -395,7 +537,8 @@ ln_bwd_generic(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
 // ---------------------------------------------------------------------------
 struct LnGeometry {
   bool vec;
-  bool smem_acc;  // backward with shared-memory accumulators (ln_bwd_cta)
+  bool smem_acc;  // backward with shared-memory accumulators (ln_bwd_cta / ln_bwd_grp)
+  bool grouped;   // backward: ln_bwd_grp (several 64-thread row groups per block)
   int tpr, vpt, block, rpc, bps;
 };
 
@@ -414,10 +557,10 @@ LnGeometry ln_geometry(int64_t H, size_t io_size, bool bwd) {
   }
   g.vec = true;
   // Backward (2 vectors per thread): rows of up to 64 vectors take a warp per
-  // row and rows of up to 128 a 64-thread block per row, both with register
-  // accumulators; wider rows one block per row with the accumulators in shared
-  // memory (ln_bwd_cta: at most 64 registers, 1024 threads per SM).  Blocks per
-  // SM set P, the number of [dW | dB] partial rows.
+  // row with register accumulators; rows of up to 128 a 64-thread row group,
+  // four groups per block (ln_bwd_grp); wider rows one block per row (ln_bwd_cta);
+  // both keep the accumulators in shared memory (at most 64 registers, 1024
+  // threads per SM).  Blocks per SM set P, the number of [dW | dB] partial rows.
   const int64_t warp_limit = bwd ? 64 : 32LL * max_vpt;
   if (nvec <= warp_limit) {
     g.tpr = 32;
@@ -432,9 +575,14 @@ LnGeometry ln_geometry(int64_t H, size_t io_size, bool bwd) {
     g.vpt = max_vpt;
     g.block = tpr;
     g.rpc = 1;
-    g.smem_acc = bwd && nvec > 128;
-    const int threads_per_sm = g.smem_acc ? 1024 : 512;
-    g.bps = threads_per_sm / tpr > 0 ? threads_per_sm / tpr : 1;
+    g.smem_acc = bwd;
+    g.bps = 1024 / tpr;
+    if (bwd && tpr == kLnGroupThreads) {  // 65..128 vectors: grouped blocks
+      g.grouped = true;
+      g.block = kLnGroups * kLnGroupThreads;
+      g.rpc = kLnGroups;
+      g.bps = 1024 / g.block;
+    }
   }
   return g;
 }
@@ -539,6 +687,36 @@ gbln_status ln_bwd_cta_launch(bool dres, unsigned P, const void* dy, const void*
 }
 
 template <typename T, typename W>
+gbln_status ln_bwd_grp_launch(bool dres, unsigned P, const void* dy, const void* dr, const void* h,
+                              const void* w, const float* mean, const float* rstd, void* dx,
+                              float* partial, int64_t rows, int H, float inv_H, cudaStream_t s) {
+  constexpr int VPT = 2;
+  const size_t smem = (size_t)kLnGroups * 2 * VPT * VecOf<T>::N * kLnGroupThreads * sizeof(float);
+  static std::atomic<uint64_t> attr_done{0};  // one bit per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return GBLN_ERR_CUDA; }
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+    if (cudaFuncSetAttribute(ln_bwd_grp<T, W, VPT, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(ln_bwd_grp<T, W, VPT, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+      cudaGetLastError();
+      return GBLN_ERR_CUDA;
+    }
+    attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  constexpr int B = kLnGroups * kLnGroupThreads;
+  if (dres)
+    ln_bwd_grp<T, W, VPT, true><<<P, B, smem, s>>>(
+        (const T*)dy, (const T*)dr, (const T*)h, (const W*)w, mean, rstd, (T*)dx, partial, rows, H, inv_H);
+  else
+    ln_bwd_grp<T, W, VPT, false><<<P, B, smem, s>>>(
+        (const T*)dy, nullptr, (const T*)h, (const W*)w, mean, rstd, (T*)dx, partial, rows, H, inv_H);
+  return GBLN_OK;
+}
+
+template <typename T, typename W>
 gbln_status ln_bwd_typed(const void* dy, const void* dr, const void* h, const void* w,
                          const float* mean, const float* rstd, void* dx, float* partial, int64_t P,
                          int64_t rows, int64_t H, cudaStream_t s) {
@@ -561,12 +739,12 @@ gbln_status ln_bwd_typed(const void* dy, const void* dr, const void* h, const vo
   if (g.tpr == 32) {
     if (g.vpt == 1) ln_bwd_vec_launch<T, W, 32, 1, kLnWarpBlock>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s);
     else ln_bwd_vec_launch<T, W, 32, 2, kLnWarpBlock>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s);
-  } else if (!g.smem_acc) {
-    ln_bwd_vec_launch<T, W, 64, 2, 64>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s);
+  } else if (g.grouped) {
+    const gbln_status st = ln_bwd_grp_launch<T, W>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s);
+    if (st != GBLN_OK) return st;
   } else {
     gbln_status st = GBLN_OK;
     switch (g.tpr) {
-      case 64: st = ln_bwd_cta_launch<T, W, 64, 2>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
       case 128: st = ln_bwd_cta_launch<T, W, 128, 2>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
       case 256: st = ln_bwd_cta_launch<T, W, 256, 2>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
       default: st = ln_bwd_cta_launch<T, W, 512, 2>(dres, grid, dy, dr, h, w, mean, rstd, dx, partial, rows, hh, inv_H, s); break;
@@ -645,10 +823,9 @@ extern "C" gbln_status gbln_layernorm_dwdb_finalize(const float* dwdb_partial, i
   if (P < 0 || H <= 0 || H > kMaxH) return GBLN_ERR_INVALID_ARG;
   if (!dw || !db || (P > 0 && !dwdb_partial)) return GBLN_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  const unsigned grid = (unsigned)((H + 31) / 32);
   const int acc = accumulate ? 1 : 0;
-  colsum_kernel<<<grid, 32 * kColSumStripes, 0, s>>>(dwdb_partial, P, (int)H, (int)(2 * H), dw, acc);
-  colsum_kernel<<<grid, 32 * kColSumStripes, 0, s>>>(P > 0 ? dwdb_partial + H : nullptr, P, (int)H,
-                                                     (int)(2 * H), db, acc);
+  // one launch over the 2H columns [dW | dB] of the partial rows
+  colsum_kernel<<<(unsigned)((2 * H + 31) / 32), 32 * kColSumStripes, 0, s>>>(
+      dwdb_partial, P, (int)(2 * H), (int)(2 * H), dw, db, (int)H, acc);
   return launch_status();
 }

@@ -245,6 +245,125 @@ rms_bwd_vec(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
 // Backward, element-wise path: P blocks, each over its contiguous row chunk,
 // one row at a time; thread t owns columns t, t+256, ... of the partial row.
 // ---------------------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// Backward for rows of 65..128 vectors: kRmsGroups row groups of 64 threads (two
+// vectors per thread) per block, the dW accumulators of each group in shared
+// memory (four consecutive columns of a thread per 16-byte slot, slot k of
+// thread t at acc[k * 64 + t]), a named barrier per group for its row sums.
+// At 64 registers 1024 threads stay resident per SM (the warp-per-row kernel
+// holds four vectors and the accumulators in ~124 registers: 512 threads).
+// Groups walk rows r0 + g, r0 + g + kRmsGroups, ...; their accumulators are
+// summed in a fixed order at the end.
+// ---------------------------------------------------------------------------
+constexpr int kRmsGroups = 4;
+constexpr int kRmsGroupThreads = 64;
+
+template <typename T, typename W, bool DRES>
+__global__ void __launch_bounds__(kRmsGroups * kRmsGroupThreads, 1024 / (kRmsGroups * kRmsGroupThreads))
+rms_bwd_grp(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
+            const float* __restrict__ rstd, T* dx, float* __restrict__ partial,
+            int64_t rows, int H, float inv_H) {
+  constexpr int TPR = kRmsGroupThreads, VPT = 2;
+  constexpr int VEC = VecOf<T>::N;
+  constexpr int Q = VEC / 4;
+  constexpr int NSL = VPT * Q;
+  extern __shared__ float4 acc_all[];  // [kRmsGroups][NSL][TPR]
+  __shared__ float red[kRmsGroups][2][TPR / 32];
+  const int g = threadIdx.x / TPR, l = threadIdx.x % TPR, lane = threadIdx.x % 32;
+  float4* acc = acc_all + (size_t)g * NSL * TPR;
+  const int nvec = H / VEC;
+  const int64_t P = gridDim.x, p = blockIdx.x;
+  const int64_t r0 = p * rows / P, r1 = (p + 1) * rows / P;
+#pragma unroll
+  for (int k = 0; k < NSL; ++k) acc[k * TPR + l] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+  int par = 0;
+  for (int64_t row = r0 + g; row < r1; row += kRmsGroups) {
+    const size_t base = (size_t)row * H;
+    uint4 dya[VPT], ha[VPT], dra[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int iv = l + v * TPR;
+      if (iv < nvec) {
+        dya[v] = ld_stream(dy + base + (size_t)iv * VEC);
+        ha[v] = ld_stream(h + base + (size_t)iv * VEC);
+        if constexpr (DRES) dra[v] = ld_stream(dres + base + (size_t)iv * VEC);
+      }
+    }
+    const float rs = rstd[row];
+    float dot = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int iv = l + v * TPR;
+      if (iv < nvec) {
+        float d[VEC], n[VEC], wv[VEC];
+        unpack<VEC>(dya[v], d);
+        unpack<VEC>(ha[v], n);
+        load_weight<W, VEC>(w, iv, wv);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          n[e] *= rs;
+          dot = fmaf(d[e] * wv[e], n[e], dot);
+        }
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+          float4* aw = acc + (v * Q + q) * TPR + l;
+          float4 a = *aw;
+          a.x = fmaf(d[4 * q], n[4 * q], a.x);
+          a.y = fmaf(d[4 * q + 1], n[4 * q + 1], a.y);
+          a.z = fmaf(d[4 * q + 2], n[4 * q + 2], a.z);
+          a.w = fmaf(d[4 * q + 3], n[4 * q + 3], a.w);
+          *aw = a;
+        }
+      }
+    }
+    // Row sum over the group's two warps; red is double-buffered by row parity
+    // (a buffer is written again only after the group's next barrier, which
+    // every thread reaches after reading it).
+    dot = group_sum<32>(dot);
+    if (lane == 0) red[g][par][l / 32] = dot;
+    bar_sync_named(1 + g, TPR);
+    float tot = red[g][par][0];
+#pragma unroll
+    for (int k = 1; k < TPR / 32; ++k) tot += red[g][par][k];
+    par ^= 1;
+    const float c = tot * inv_H;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int iv = l + v * TPR;
+      if (iv < nvec) {
+        float d[VEC], n[VEC], wv[VEC], o[VEC];
+        unpack<VEC>(dya[v], d);
+        unpack<VEC>(ha[v], n);
+        load_weight<W, VEC>(w, iv, wv);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[e] = rs * (d[e] * wv[e] - (n[e] * rs) * c);
+        if constexpr (DRES) {
+          float d2[VEC];
+          unpack<VEC>(dra[v], d2);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) o[e] += d2[e];
+        }
+        st_vec(dx + base + (size_t)iv * VEC, pack<T, VEC>(o));
+      }
+    }
+  }
+  __syncthreads();
+  // Fixed-order sum over the groups: column j is component j % 4 of slot
+  // v * Q + (j % VEC) / 4 of thread lt, where j / VEC = lt + v * TPR.
+  float* prow = partial + (size_t)p * H;
+  const float* af = reinterpret_cast<const float*>(acc_all);
+  for (int j = threadIdx.x; j < H; j += kRmsGroups * TPR) {
+    const int iv = j / VEC, e = j % VEC;
+    const int lt = iv % TPR, v = iv / TPR;
+    const size_t sl = ((size_t)(v * Q + e / 4) * TPR + lt) * 4 + e % 4;
+    float a = 0.f;
+#pragma unroll
+    for (int q = 0; q < kRmsGroups; ++q) a += af[(size_t)q * NSL * TPR * 4 + sl];
+    prow[j] = a;
+  }
+}
+
 template <typename T, typename W, bool DRES>
 __global__ void __launch_bounds__(kGenericBlock)
 rms_bwd_generic(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
@@ -309,6 +428,20 @@ Geometry geometry(int64_t H, size_t io_size) {
     g.block = tpr;
     g.rpc = 1;
     g.bps = 512 / tpr > 0 ? 512 / tpr : 1;
+  }
+  return g;
+}
+
+// Backward geometry: rows of 65..128 vectors go to rms_bwd_grp (64-thread row
+// groups, four per block, four blocks per SM); everything else as the forward.
+Geometry bwd_geometry(int64_t H, size_t io_size) {
+  Geometry g = geometry(H, io_size);
+  if (g.vec && g.tpr == 32 && g.vpt == 4) {
+    g.tpr = kRmsGroupThreads;
+    g.vpt = 2;
+    g.block = kRmsGroups * kRmsGroupThreads;
+    g.rpc = kRmsGroups;
+    g.bps = 1024 / g.block;
   }
   return g;
 }
@@ -383,11 +516,38 @@ void bwd_vec(bool dres, unsigned P, const void* dy, const void* dr, const void* 
 }
 
 template <typename T, typename W>
+gbln_status bwd_grp(bool dres, unsigned P, const void* dy, const void* dr, const void* h,
+                    const void* w, const float* rstd, void* dx, float* partial, int64_t rows, int H,
+                    float inv_H, cudaStream_t s) {
+  const size_t smem = (size_t)kRmsGroups * 2 * VecOf<T>::N * kRmsGroupThreads * sizeof(float);
+  static std::atomic<uint64_t> attr_done{0};  // one bit per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return GBLN_ERR_CUDA; }
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+    if (cudaFuncSetAttribute(rms_bwd_grp<T, W, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(rms_bwd_grp<T, W, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+      cudaGetLastError();
+      return GBLN_ERR_CUDA;
+    }
+    attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  constexpr int B = kRmsGroups * kRmsGroupThreads;
+  if (dres)
+    rms_bwd_grp<T, W, true><<<P, B, smem, s>>>(
+        (const T*)dy, (const T*)dr, (const T*)h, (const W*)w, rstd, (T*)dx, partial, rows, H, inv_H);
+  else
+    rms_bwd_grp<T, W, false><<<P, B, smem, s>>>(
+        (const T*)dy, nullptr, (const T*)h, (const W*)w, rstd, (T*)dx, partial, rows, H, inv_H);
+  return launch_status();
+}
+
+template <typename T, typename W>
 gbln_status bwd_typed(const void* dy, const void* dr, const void* h, const void* w,
                       const float* rstd, void* dx, float* partial, int64_t P, int64_t rows,
                       int64_t H, cudaStream_t s) {
   const bool dres = dr != nullptr;
-  const Geometry g = geometry(H, sizeof(T));
+  const Geometry g = bwd_geometry(H, sizeof(T));
   const bool vec = g.vec && aligned16(dy) && aligned16(h) && aligned16(w) && aligned16(dx) &&
                    aligned16(partial) && (!dres || aligned16(dr));
   const float inv_H = 1.0f / (float)H;
@@ -404,8 +564,9 @@ gbln_status bwd_typed(const void* dy, const void* dr, const void* h, const void*
   }
   if (g.tpr == 32) {
     if (g.vpt == 1) bwd_vec<T, W, 32, 1, kWarpBlock>(dres, grid, dy, dr, h, w, rstd, dx, partial, rows, hh, inv_H, s);
-    else if (g.vpt == 2) bwd_vec<T, W, 32, 2, kWarpBlock>(dres, grid, dy, dr, h, w, rstd, dx, partial, rows, hh, inv_H, s);
-    else bwd_vec<T, W, 32, 4, kWarpBlock>(dres, grid, dy, dr, h, w, rstd, dx, partial, rows, hh, inv_H, s);
+    else bwd_vec<T, W, 32, 2, kWarpBlock>(dres, grid, dy, dr, h, w, rstd, dx, partial, rows, hh, inv_H, s);
+  } else if (g.rpc == kRmsGroups) {
+    return bwd_grp<T, W>(dres, grid, dy, dr, h, w, rstd, dx, partial, rows, hh, inv_H, s);
   } else {
     switch (g.tpr) {
       case 64: bwd_vec<T, W, 64, 4, 64>(dres, grid, dy, dr, h, w, rstd, dx, partial, rows, hh, inv_H, s); break;
@@ -475,7 +636,7 @@ extern "C" int64_t gbln_rmsnorm_bwd_num_partials(int64_t T, int64_t H, gbln_dtyp
   if (T == 0) return 0;
   const int sms = sm_count();
   if (sms <= 0) return -1;
-  return partials_for(T, geometry(H, dtype_size(io)), sms);
+  return partials_for(T, bwd_geometry(H, dtype_size(io)), sms);
 }
 
 extern "C" gbln_status gbln_rmsnorm_bwd(const void* dy, const void* dresidual_out, const void* h,
@@ -489,7 +650,7 @@ extern "C" gbln_status gbln_rmsnorm_bwd(const void* dy, const void* dresidual_ou
   if (!dy || !h || !weight || !rstd || !dx || !dw_partial) return GBLN_ERR_INVALID_ARG;
   const int sms = sm_count();
   if (sms <= 0) return GBLN_ERR_CUDA;
-  const int64_t P = partials_for(T, geometry(H, dtype_size(io)), sms);
+  const int64_t P = partials_for(T, bwd_geometry(H, dtype_size(io)), sms);
   if (P_cap < P) return GBLN_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
   if (io == GBLN_F32)
@@ -505,8 +666,8 @@ extern "C" gbln_status gbln_rmsnorm_dw_finalize(const float* dw_partial, int64_t
   if (P < 0 || H <= 0 || H > kMaxH) return GBLN_ERR_INVALID_ARG;
   if (!dw || (P > 0 && !dw_partial)) return GBLN_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  const unsigned grid = (unsigned)((H + 31) / 32);
-  colsum_kernel<<<grid, 32 * kColSumStripes, 0, s>>>(dw_partial, P, (int)H, (int)H, dw, accumulate ? 1 : 0);
+  colsum_kernel<<<(unsigned)((H + 31) / 32), 32 * kColSumStripes, 0, s>>>(
+      dw_partial, P, (int)H, (int)H, dw, dw, (int)H, accumulate ? 1 : 0);
   return launch_status();
 }
 
@@ -565,7 +726,7 @@ extern "C" gbln_status gbln_rmsnorm_bwd_noalloc(const void* dy, const void* dres
   if (!dw) return GBLN_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   if (T == 0) {  // no rows: dW = 0
-    colsum_kernel<<<(unsigned)((H + 31) / 32), 32 * kColSumStripes, 0, s>>>(nullptr, 0, (int)H, (int)H, dw, 0);
+    colsum_kernel<<<(unsigned)((H + 31) / 32), 32 * kColSumStripes, 0, s>>>(nullptr, 0, (int)H, (int)H, dw, dw, (int)H, 0);
     return launch_status();
   }
   if (!dy || !h || !weight || !rstd || !dx) return GBLN_ERR_INVALID_ARG;
@@ -575,7 +736,7 @@ extern "C" gbln_status gbln_rmsnorm_bwd_noalloc(const void* dy, const void* dres
   if (!scratch) return GBLN_ERR_CUDA;
   // Same kernels as gbln_rmsnorm_bwd + gbln_rmsnorm_dw_finalize; fewer partial
   // rows when the usual count would not fit the fixed array.
-  int64_t P = partials_for(T, geometry(H, dtype_size(io)), sms);
+  int64_t P = partials_for(T, bwd_geometry(H, dtype_size(io)), sms);
   if (P * H > kScratchFloats) P = kScratchFloats / H;
   gbln_status st;
   if (io == GBLN_F32)
@@ -585,6 +746,6 @@ extern "C" gbln_status gbln_rmsnorm_bwd_noalloc(const void* dy, const void* dres
   else
     st = bwd_typed<bf16, float>(dy, dresidual_out, h, weight, rstd, dx, scratch, P, T, H, s);
   if (st != GBLN_OK) return st;
-  colsum_kernel<<<(unsigned)((H + 31) / 32), 32 * kColSumStripes, 0, s>>>(scratch, P, (int)H, (int)H, dw, 0);
+  colsum_kernel<<<(unsigned)((H + 31) / 32), 32 * kColSumStripes, 0, s>>>(scratch, P, (int)H, (int)H, dw, dw, (int)H, 0);
   return launch_status();
 }
