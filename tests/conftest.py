@@ -27,3 +27,16 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _device_error_word_stays_clear():
+    """After every module that loaded the library on a GPU: no kernel may have
+    given up on a bounded wait (the per-device error word stays 0)."""
+    yield
+    mod = sys.modules.get("rmsnorm_fwd_bwd_03_gb300")
+    if mod is None or getattr(mod, "_lib", None) is None or not gpu_available():
+        return
+    import torch
+    torch.cuda.synchronize()
+    assert mod.device_error() == 0, "a kernel reported a wait timeout (device error word != 0)"
