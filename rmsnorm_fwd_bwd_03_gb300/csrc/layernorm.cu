@@ -115,7 +115,7 @@ ln_fwd_generic(const T* x, const T* r, const W* __restrict__ w, const W* __restr
   __shared__ float red[kLnGenericBlock / 32];
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
     const size_t base = (size_t)row * H;
-    float s1 = 0.f;
+    KahanSum s1;
     for (int j = threadIdx.x; j < H; j += kLnGenericBlock) {
       float a = to_f32(x[base + j]);
       if constexpr (RES) {
@@ -123,15 +123,15 @@ ln_fwd_generic(const T* x, const T* r, const W* __restrict__ w, const W* __restr
         hout[base + j] = hv;
         a = to_f32(hv);
       }
-      s1 += a;
+      s1.add(a);
     }
-    const float mu = row_sum<kLnGenericBlock>(s1, red) * inv_H;
-    float s2 = 0.f;
+    const float mu = row_sum<kLnGenericBlock>(s1.s, red) * inv_H;
+    KahanSum s2;
     for (int j = threadIdx.x; j < H; j += kLnGenericBlock) {
       const float c = (RES ? to_f32(hout[base + j]) : to_f32(x[base + j])) - mu;  // own write
-      s2 = fmaf(c, c, s2);
+      s2.add(c * c);
     }
-    const float rs = rsqrtf(row_sum<kLnGenericBlock>(s2, red) * inv_H + eps);
+    const float rs = rsqrtf(row_sum<kLnGenericBlock>(s2.s, red) * inv_H + eps);
     if (threadIdx.x == 0) {
       mean_out[row] = mu;
       rstd[row] = rs;
@@ -512,14 +512,14 @@ ln_bwd_generic(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
   for (int64_t row = r0; row < r1; ++row) {
     const size_t base = (size_t)row * H;
     const float mu = mean[row], rs = rstd[row];
-    float sg = 0.f, sgn = 0.f;
+    KahanSum sg, sgn;
     for (int j = threadIdx.x; j < H; j += kLnGenericBlock) {
       const float gg = to_f32(dy[base + j]) * to_f32(w[j]);
-      sg += gg;
-      sgn = fmaf(gg, (to_f32(h[base + j]) - mu) * rs, sgn);
+      sg.add(gg);
+      sgn.add(gg * ((to_f32(h[base + j]) - mu) * rs));
     }
-    const float mg = row_sum<kLnGenericBlock>(sg, red) * inv_H;
-    const float mgn = row_sum<kLnGenericBlock>(sgn, red) * inv_H;
+    const float mg = row_sum<kLnGenericBlock>(sg.s, red) * inv_H;
+    const float mgn = row_sum<kLnGenericBlock>(sgn.s, red) * inv_H;
     for (int j = threadIdx.x; j < H; j += kLnGenericBlock) {
       const float d = to_f32(dy[base + j]);
       const float n = (to_f32(h[base + j]) - mu) * rs;

@@ -105,7 +105,7 @@ rms_fwd_generic(const T* x, const T* r, const W* __restrict__ w, T* y, T* hout,
   __shared__ float red[kGenericBlock / 32];
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
     const size_t base = (size_t)row * H;
-    float ss = 0.f;
+    KahanSum ks;
     for (int j = threadIdx.x; j < H; j += kGenericBlock) {
       float a = to_f32(x[base + j]);
       if constexpr (RES) {
@@ -113,9 +113,9 @@ rms_fwd_generic(const T* x, const T* r, const W* __restrict__ w, T* y, T* hout,
         hout[base + j] = hv;
         a = to_f32(hv);
       }
-      ss = fmaf(a, a, ss);
+      ks.add(a * a);
     }
-    ss = row_sum<kGenericBlock>(ss, red);
+    const float ss = row_sum<kGenericBlock>(ks.s, red);
     const float rs = rsqrtf(ss * inv_H + eps);
     if (threadIdx.x == 0) rstd[row] = rs;
     // With MX, H is a multiple of 32, so each warp's pass covers one MX block.
@@ -377,10 +377,10 @@ rms_bwd_generic(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
   for (int64_t row = r0; row < r1; ++row) {
     const size_t base = (size_t)row * H;
     const float rs = rstd[row];
-    float dot = 0.f;
+    KahanSum kd;
     for (int j = threadIdx.x; j < H; j += kGenericBlock)
-      dot = fmaf(to_f32(dy[base + j]) * to_f32(w[j]), to_f32(h[base + j]) * rs, dot);
-    dot = row_sum<kGenericBlock>(dot, red);
+      kd.add(to_f32(dy[base + j]) * to_f32(w[j]) * (to_f32(h[base + j]) * rs));
+    const float dot = row_sum<kGenericBlock>(kd.s, red);
     const float c = dot * inv_H;
     for (int j = threadIdx.x; j < H; j += kGenericBlock) {
       const float d = to_f32(dy[base + j]);

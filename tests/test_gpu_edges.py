@@ -67,6 +67,28 @@ def test_rmsnorm_shapes(T, H, io, wt, residual, offset):
     check_dw(to64(dw), dw_ref)
 
 
+def test_rmsnorm_largest_row():
+    # H = 2^24, the largest width the entry points accept: one block per row on the
+    # element-wise kernels, a single partial row.
+    T, H = 1, 1 << 24
+    x = _randn((T, H), torch.bfloat16, 6)
+    r = _randn((T, H), torch.bfloat16, 7)
+    w = (1 + 0.1 * _randn((H,), torch.float32, 8))
+    dy = _randn((T, H), torch.bfloat16, 9)
+    y, h, rstd = gb.rmsnorm_fwd(x, w, 1e-5, r)
+    dx, part, P = gb.rmsnorm_bwd(dy, h, w, rstd, None)
+    dw = gb.rmsnorm_dw_finalize(part, P)
+    torch.cuda.synchronize()
+    w64 = to64(w)
+    y_ref, h_ref, rstd_ref = oracle.rmsnorm_fwd(to64(x), to64(r), w64, 1e-5, io="bf16")
+    assert np.array_equal(to64(h), h_ref)
+    check_io(to64(y), y_ref, "bf16", "y")
+    check_rstd(to64(rstd), rstd_ref)
+    dx_ref, dw_ref = oracle.rmsnorm_bwd(to64(dy), None, h_ref, w64, 1e-5)
+    check_io(to64(dx), dx_ref, "bf16", "dx")
+    check_dw(to64(dw), dw_ref)
+
+
 def test_rmsnorm_outlier_channels_and_large_eps():
     T, H = 64, 4096
     x = _randn((T, H), torch.bfloat16, 11)
@@ -180,6 +202,37 @@ def test_rope_shapes(T, Hq, Hk, D, io, offset):
     if Hk:
         check_io(to64(ko), oracle.rope_fwd(to64(k), p, theta), io, "k'")
         check_io(to64(dki), oracle.rope_bwd(to64(k), p, theta), io, "dk")
+
+
+@pytest.mark.parametrize("D,offset", [(8192, 0), (1024, 1)])
+def test_rope_largest_heads(D, offset):
+    # The largest head sizes: D = 8192 on the bf16 vector path (512 units of 8
+    # elements per head half), D = 1024 on the element-wise path (512 units).
+    T, dt, theta = 3, torch.bfloat16, 10000.0
+    q = _randn((T, 1, D), dt, 61, offset=offset)
+    k = _randn((T, 1, D), dt, 62, offset=offset)
+    pos = torch.tensor([0, 7, 4095], dtype=torch.int32, device="cuda")
+    table = gb.rope_table(4096, D, theta)
+    qo, ko = gb.rope_fwd(q, k, pos, table)
+    torch.cuda.synchronize()
+    p = pos.cpu().numpy()
+    check_io(to64(qo), oracle.rope_fwd(to64(q), p, theta), "bf16", "q'")
+    check_io(to64(ko), oracle.rope_fwd(to64(k), p, theta), "bf16", "k'")
+
+
+def test_rope_head_size_beyond_the_kernels_is_unsupported():
+    # one unit more than either path takes: 513 vector units (bf16, D = 8208) and
+    # 513 element units (unaligned, D = 1026)
+    lib = gb.library()
+    s = torch.cuda.current_stream().cuda_stream
+    pos = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for D, off in ((8208, 0), (1026, 1)):
+        q = _randn((D + 8,), torch.bfloat16, 63)
+        table = gb.rope_table(1, D, 10000.0)
+        qp = q.data_ptr() + 2 * off
+        st = lib.gbln_rope_fwd(qp, None, qp, None, pos.data_ptr(), table.data_ptr(), 1, 1, 1, 0, D,
+                               gb.BF16, s)
+        assert st == 2, (D, st)  # GBLN_ERR_UNSUPPORTED
 
 
 def test_rope_table_values():

@@ -74,6 +74,31 @@ def test_layernorm_shapes(T, H, io, wt, opts, offset):
     check_dw(to64(db), db_ref, "dB")
 
 
+def test_layernorm_largest_row():
+    # H = 2^24, the largest accepted width: element-wise kernels with long
+    # per-thread sums (compensated), one partial row.
+    T, H = 1, 1 << 24
+    dt = torch.bfloat16
+    x = _randn((T, H), dt, 21, 2.0, 0.5)
+    r = _randn((T, H), dt, 22)
+    w = (1 + 0.1 * _randn((H,), torch.float32, 23))
+    b = _randn((H,), torch.float32, 24)
+    dy = _randn((T, H), dt, 25)
+    y, h, mean, rstd = gb.layernorm_fwd(x, w, 1e-5, r, b)
+    dx, part, P = gb.layernorm_bwd(dy, h, w, mean, rstd)
+    dw, db = gb.layernorm_dwdb_finalize(part, P)
+    torch.cuda.synchronize()
+    y_ref, h_ref, mean_ref, rstd_ref = oracle.layernorm_fwd(to64(x), to64(r), to64(w), to64(b), 1e-5, io="bf16")
+    assert np.array_equal(to64(h), h_ref)
+    check_io(to64(y), y_ref, "bf16", "y")
+    check_rstd(to64(rstd), rstd_ref)
+    assert np.allclose(to64(mean), mean_ref, rtol=1e-5, atol=1e-6 * np.max(np.abs(h_ref)))
+    dx_ref, dw_ref, db_ref = oracle.layernorm_bwd(to64(dy), None, h_ref, to64(w), 1e-5)
+    check_io(to64(dx), dx_ref, "bf16", "dx")
+    check_dw(to64(dw), dw_ref, "dW")
+    check_dw(to64(db), db_ref, "dB")
+
+
 @pytest.mark.parametrize("H", [1024, 4096])  # grouped row blocks; one block per row
 def test_layernorm_llama_width_deterministic_and_accumulate(H):
     T = 4099
