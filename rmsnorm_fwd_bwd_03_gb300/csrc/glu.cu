@@ -37,11 +37,6 @@ __device__ __forceinline__ float sigmoid(float g) {
   }
 }
 
-template <typename T>
-__device__ __forceinline__ float exp_io(float x) {
-  if constexpr (sizeof(T) == 4) return expf(x); else return __expf(x);
-}
-
 // GeLU, tanh form: 0.5 x (1 + tanh(z)) with z = sqrt(2/pi) (x + 0.044715 x^3).
 // Since 0.5 (1 + tanh(z)) = sigmoid(2 z), it is evaluated as x * sigmoid(2 z),
 // which has no cancellation for negative x.
@@ -49,6 +44,27 @@ constexpr float kGeluK = 1.5957691216057308f;   // 2 * sqrt(2 / pi)
 constexpr float kGeluC = 0.044715f;
 constexpr float kInvSqrt2 = 0.7071067811865476f;
 constexpr float kInvSqrt2Pi = 0.3989422804014327f;  // 1 / sqrt(2 pi)
+
+// Normal CDF for the bf16 path from the rational approximation of erfc in
+// Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26
+// (absolute error of erf below 1.5e-7): for z >= 0, erfc(z) ~ (a1 t + a2 t^2 +
+// a3 t^3 + a4 t^4 + a5 t^5) e^{-z^2} with t = 1 / (1 + p z).  With z = |x| /
+// sqrt(2): Phi(x) = erfc(z) / 2 for x < 0 (no cancellation) and 1 - erfc(z) / 2
+// for x >= 0.  ex receives e^{-z^2} = e^{-x^2/2}, the Gaussian density's
+// exponential, which the backward pass needs as well.  About half the
+// instructions of erff; float32 I/O keeps erff.
+constexpr float kAsP = 0.3275911f;
+constexpr float kAsA1 = 0.254829592f, kAsA2 = -0.284496736f, kAsA3 = 1.421413741f,
+                kAsA4 = -1.453152027f, kAsA5 = 1.061405429f;
+
+__device__ __forceinline__ float gauss_cdf_as(float x, float& ex) {
+  const float z = fabsf(x) * kInvSqrt2;
+  const float t = __fdividef(1.0f, fmaf(kAsP, z, 1.0f));
+  ex = __expf(-z * z);
+  const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, kAsA5, kAsA4), kAsA3), kAsA2), kAsA1);
+  const float half_erfc = 0.5f * poly * ex;
+  return x >= 0.f ? 1.0f - half_erfc : half_erfc;
+}
 
 // Activation value f(x) and, for the backward pass, f(x) and f'(x) together.
 template <typename T, int ACT>
@@ -59,7 +75,12 @@ __device__ __forceinline__ float act_f(float x) {
   } else if constexpr (ACT == GBLN_ACT_GELU_TANH) {
     return x * sigmoid<T>(kGeluK * (x + kGeluC * x * x * x));
   } else if constexpr (ACT == GBLN_ACT_GELU_ERF) {
-    return 0.5f * x * (1.0f + erff(x * kInvSqrt2));
+    if constexpr (sizeof(T) == 4) {
+      return 0.5f * x * (1.0f + erff(x * kInvSqrt2));
+    } else {
+      float ex;
+      return x * gauss_cdf_as(x, ex);
+    }
   } else {
     return x > 0.f ? x : 0.f;
   }
@@ -76,9 +97,16 @@ __device__ __forceinline__ void act_fd(float x, float& f, float& d) {
     f = x * s;
     d = s + x * s * (1.0f - s) * kGeluK * (1.0f + 3.0f * kGeluC * x * x);
   } else if constexpr (ACT == GBLN_ACT_GELU_ERF) {
-    const float cdf = 0.5f * (1.0f + erff(x * kInvSqrt2));
-    f = x * cdf;
-    d = cdf + x * kInvSqrt2Pi * exp_io<T>(-0.5f * x * x);
+    if constexpr (sizeof(T) == 4) {
+      const float cdf = 0.5f * (1.0f + erff(x * kInvSqrt2));
+      f = x * cdf;
+      d = cdf + x * kInvSqrt2Pi * expf(-0.5f * x * x);
+    } else {
+      float ex;
+      const float cdf = gauss_cdf_as(x, ex);
+      f = x * cdf;
+      d = cdf + x * kInvSqrt2Pi * ex;
+    }
   } else {
     f = x > 0.f ? x : 0.f;
     d = x > 0.f ? 1.f : 0.f;
