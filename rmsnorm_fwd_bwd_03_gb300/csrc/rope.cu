@@ -22,48 +22,71 @@ namespace gbln {
 
 namespace {
 
+// (cos, sin) of NP consecutive pairs, loaded once per token into registers and
+// reused for every head row the thread rotates for that token.  An
+// out-of-range position loads nothing: all entries are NaN, so are the outputs.
+template <int NP>
+struct CsUnit {
+  float2 c[NP];
+};
+
+// SMEM: c points into shared memory (plain loads), else into the global table
+// (read-only cached loads).  c is 16-byte aligned whenever NP is even.
+template <int NP, bool SMEM>
+__device__ __forceinline__ CsUnit<NP> load_cs(const float2* c, bool ok) {
+  CsUnit<NP> u;
+  if (!ok) {
+    const float qnan = __int_as_float(0x7fc00000);
+#pragma unroll
+    for (int i = 0; i < NP; ++i) u.c[i] = make_float2(qnan, qnan);
+    return u;
+  }
+  if constexpr (NP % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < NP; i += 2) {
+      const float4* p4 = reinterpret_cast<const float4*>(c + i);
+      const float4 f = SMEM ? *p4 : __ldg(p4);
+      u.c[i] = make_float2(f.x, f.y);
+      u.c[i + 1] = make_float2(f.z, f.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < NP; ++i) u.c[i] = SMEM ? c[i] : __ldg(c + i);
+  }
+  return u;
+}
+
 // Rotate one vector pair: elements i0.. of the first half (a) and of the second
-// half (b) of a head row, with the cos/sin entries c[0..VEC).  On the vector
+// half (b) of a head row, with the unit's cos/sin entries cs.  On the vector
 // path the work goes two elements (one 32-bit word of bf16, or two floats) at
-// a time so that only the packed inputs and one float4 of cos/sin are live.
-// TABLE_IN_SMEM: c points into shared memory (plain loads) instead of the
-// global table (read-only cached loads).
-template <typename T, int VEC, bool BWD, bool TABLE_IN_SMEM = false>
+// a time.
+template <typename T, int VEC, bool BWD>
 __device__ __forceinline__ void rotate_store(const Packed<T, VEC>& a, const Packed<T, VEC>& b,
-                                             const float2* c, bool ok, T* d1, T* d2) {
-  const float qnan = __int_as_float(0x7fc00000);
+                                             const CsUnit<VEC>& cs, T* d1, T* d2) {
   if constexpr (VEC * sizeof(T) == 16) {
     const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a.r);
     const uint32_t* bw = reinterpret_cast<const uint32_t*>(&b.r);
     uint32_t o1[4], o2[4];
+    constexpr int PER = sizeof(T) == 2 ? 2 : 1;  // elements per 32-bit word
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       float x1[2], x2[2];
-      if constexpr (sizeof(T) == 2) {
+      if constexpr (PER == 2) {
         x1[0] = bf16_lo(aw[w]); x1[1] = bf16_hi(aw[w]);
         x2[0] = bf16_lo(bw[w]); x2[1] = bf16_hi(bw[w]);
       } else {
         x1[0] = __uint_as_float(aw[w]); x2[0] = __uint_as_float(bw[w]);
       }
-      constexpr int PER = sizeof(T) == 2 ? 2 : 1;  // elements per 32-bit word
-      float cv[2], sv[2];
-      if constexpr (PER == 2) {
-        const float4* c4 = reinterpret_cast<const float4*>(c + 2 * w);
-        const float4 f = ok ? (TABLE_IN_SMEM ? *c4 : __ldg(c4)) : make_float4(qnan, qnan, qnan, qnan);
-        cv[0] = f.x; sv[0] = f.y; cv[1] = f.z; sv[1] = f.w;
-      } else {
-        const float2 f = ok ? (TABLE_IN_SMEM ? c[w] : __ldg(c + w)) : make_float2(qnan, qnan);
-        cv[0] = f.x; sv[0] = f.y;
-      }
       float y1[2], y2[2];
 #pragma unroll
       for (int e = 0; e < PER; ++e) {
+        const float2 f = cs.c[PER * w + e];
         if constexpr (!BWD) {
-          y1[e] = x1[e] * cv[e] - x2[e] * sv[e];
-          y2[e] = x2[e] * cv[e] + x1[e] * sv[e];
+          y1[e] = x1[e] * f.x - x2[e] * f.y;
+          y2[e] = x2[e] * f.x + x1[e] * f.y;
         } else {
-          y1[e] = x1[e] * cv[e] + x2[e] * sv[e];
-          y2[e] = x2[e] * cv[e] - x1[e] * sv[e];
+          y1[e] = x1[e] * f.x + x2[e] * f.y;
+          y2[e] = x2[e] * f.x - x1[e] * f.y;
         }
       }
       if constexpr (PER == 2) {
@@ -82,7 +105,7 @@ __device__ __forceinline__ void rotate_store(const Packed<T, VEC>& a, const Pack
     b.get(x2);
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
-      const float2 f = ok ? (TABLE_IN_SMEM ? c[e] : __ldg(c + e)) : make_float2(qnan, qnan);
+      const float2 f = cs.c[e];
       if constexpr (!BWD) {
         y1[e] = x1[e] * f.x - x2[e] * f.y;
         y2[e] = x2[e] * f.x + x1[e] * f.y;
@@ -97,16 +120,15 @@ __device__ __forceinline__ void rotate_store(const Packed<T, VEC>& a, const Pack
 }
 
 // Interleaved pairing: one vector of N elements holds N/2 pairs (2m, 2m + 1),
-// rotated with cos/sin entries c[0..N/2).
-template <typename T, int N, bool BWD, bool TABLE_IN_SMEM = false>
-__device__ __forceinline__ void rotate_il_store(const Packed<T, N>& a, const float2* c, bool ok,
+// rotated with the unit's cos/sin entries cs.
+template <typename T, int N, bool BWD>
+__device__ __forceinline__ void rotate_il_store(const Packed<T, N>& a, const CsUnit<(N >= 2 ? N / 2 : 1)>& cs,
                                                 T* d) {
-  const float qnan = __int_as_float(0x7fc00000);
   float x[N], y[N];
   a.get(x);
 #pragma unroll
   for (int m = 0; m < N / 2; ++m) {
-    const float2 f = ok ? (TABLE_IN_SMEM ? c[m] : __ldg(c + m)) : make_float2(qnan, qnan);
+    const float2 f = cs.c[m];
     const float x0 = x[2 * m], x1 = x[2 * m + 1];
     if constexpr (!BWD) {
       y[2 * m] = x0 * f.x - x1 * f.y;
@@ -117,6 +139,44 @@ __device__ __forceinline__ void rotate_il_store(const Packed<T, N>& a, const flo
     }
   }
   store_n<T, N>(d, y);
+}
+
+// The same rotations reading cos/sin from shared memory as they go, one
+// 16-byte piece per pair of elements, for threads that rotate a single head
+// row per token (nothing to reuse; fewer live registers than CsUnit).
+template <typename T, int VEC, bool BWD>
+__device__ __forceinline__ void rotate_store_smem(const Packed<T, VEC>& a, const Packed<T, VEC>& b,
+                                                  const float2* c, bool ok, T* d1, T* d2) {
+  if constexpr (VEC * sizeof(T) == 16 && sizeof(T) == 2) {
+    const float qnan = __int_as_float(0x7fc00000);
+    const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a.r);
+    const uint32_t* bw = reinterpret_cast<const uint32_t*>(&b.r);
+    uint32_t o1[4], o2[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float4 f = ok ? *reinterpret_cast<const float4*>(c + 2 * w) : make_float4(qnan, qnan, qnan, qnan);
+      const float x1[2] = {bf16_lo(aw[w]), bf16_hi(aw[w])};
+      const float x2[2] = {bf16_lo(bw[w]), bf16_hi(bw[w])};
+      const float cv[2] = {f.x, f.z}, sv[2] = {f.y, f.w};
+      float y1[2], y2[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        if constexpr (!BWD) {
+          y1[e] = x1[e] * cv[e] - x2[e] * sv[e];
+          y2[e] = x2[e] * cv[e] + x1[e] * sv[e];
+        } else {
+          y1[e] = x1[e] * cv[e] + x2[e] * sv[e];
+          y2[e] = x2[e] * cv[e] - x1[e] * sv[e];
+        }
+      }
+      o1[w] = pack_bf16x2(y1[0], y1[1]);
+      o2[w] = pack_bf16x2(y2[0], y2[1]);
+    }
+    st_vec(d1, make_uint4(o1[0], o1[1], o1[2], o1[3]));
+    st_vec(d2, make_uint4(o2[0], o2[1], o2[2], o2[3]));
+  } else {
+    rotate_store<T, VEC, BWD>(a, b, load_cs<VEC, true>(c, ok), d1, d2);
+  }
 }
 
 // Everything a RoPE launch needs.  ld* are token strides in elements (a head
@@ -157,6 +217,7 @@ rope_kernel(const RopeArgs<T> A, int HP) {
   const int HT = A.Hq + A.Hk;
   const int i0 = v * VEC;                 // first element of the unit
   const int c0 = IL ? i0 / 2 : i0;        // first cos/sin entry of the unit
+  constexpr int NP = IL ? (VEC >= 2 ? VEC / 2 : 1) : VEC;  // cos/sin pairs of the unit
   for (int64_t tb = (int64_t)blockIdx.x * UT; tb < A.rows; tb += (int64_t)gridDim.x * UT) {
     int p[UT];
 #pragma unroll
@@ -182,16 +243,16 @@ rope_kernel(const RopeArgs<T> A, int HP) {
         if (t >= A.rows) break;
         // out-of-range position: the table is not read and the outputs are NaN
         const bool ok = p[u] >= 0 && (int64_t)p[u] < A.max_pos;
-        const float2* c = A.cs + (ok ? (size_t)p[u] * half : 0) + c0;
+        const CsUnit<NP> cs = load_cs<NP, false>(A.cs + (ok ? (size_t)p[u] * half : 0) + c0, ok);
 #pragma unroll
         for (int j = 0; j < HPT; ++j) {
           const int h = h0 + j * HP;
           if (h < HT) {
             T* dst = A.dst(t, h);
             if constexpr (IL)
-              rotate_il_store<T, VEC, BWD>(a[u][j], c, ok, dst + i0);
+              rotate_il_store<T, VEC, BWD>(a[u][j], cs, dst + i0);
             else
-              rotate_store<T, VEC, BWD>(a[u][j], b[u][j], c, ok, dst + i0, dst + half + i0);
+              rotate_store<T, VEC, BWD>(a[u][j], b[u][j], cs, dst + i0, dst + half + i0);
           }
         }
       }
@@ -238,7 +299,7 @@ __host__ __device__ inline StageGeom stage_geom(int Hq, int Hk, int D, int TT) {
 // contiguous Q (K) rows a tile's rows are one bulk copy, otherwise one per
 // token.  Consumer thread (r, v): unit v of the head rows, head lanes r,
 // r + HPL, ... (a unit as in the register path).
-template <typename T, bool BWD, bool IL>
+template <typename T, bool BWD, bool IL, bool HOIST>
 __global__ void __launch_bounds__(kStagedMaxThreads)
 rope_staged_kernel(const RopeArgs<T> A, int TT, int HPL, unsigned int* err) {
   constexpr int VEC = VecOf<T>::N;
@@ -318,6 +379,7 @@ rope_staged_kernel(const RopeArgs<T> A, int TT, int HPL, unsigned int* err) {
   const bool active = r < HPL;
   const int i0 = v * VEC;
   const int c0 = IL ? i0 / 2 : i0;
+  constexpr int NP = IL ? (VEC >= 2 ? VEC / 2 : 1) : VEC;  // cos/sin pairs of a unit
   int64_t j = 0;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
     const int st = (int)(j % kRopeStages);
@@ -337,6 +399,8 @@ rope_staged_kernel(const RopeArgs<T> A, int TT, int HPL, unsigned int* err) {
         const int64_t t = t0 + tok;
         const bool ok = spos[tok] >= 0;
         const float2* cc = scs + (size_t)tok * half + c0;
+        CsUnit<NP> cs;
+        if constexpr (HOIST) cs = load_cs<NP, true>(cc, ok);
         for (int h = r; h < HT; h += HPL) {
           const T* src = reinterpret_cast<const T*>(h < Hq ? sq + (size_t)tok * g.qrow
                                                            : sk + (size_t)tok * g.krow) +
@@ -345,11 +409,13 @@ rope_staged_kernel(const RopeArgs<T> A, int TT, int HPL, unsigned int* err) {
           Packed<T, VEC> a;
           a.r = ld_shared_v4(src + i0);
           if constexpr (IL) {
-            rotate_il_store<T, VEC, BWD, true>(a, cc, ok, dst + i0);
+            if constexpr (HOIST) rotate_il_store<T, VEC, BWD>(a, cs, dst + i0);
+            else rotate_il_store<T, VEC, BWD>(a, load_cs<NP, true>(cc, ok), dst + i0);
           } else {
             Packed<T, VEC> b;
             b.r = ld_shared_v4(src + half + i0);
-            rotate_store<T, VEC, BWD, true>(a, b, cc, ok, dst + i0, dst + half + i0);
+            if constexpr (HOIST) rotate_store<T, VEC, BWD>(a, b, cs, dst + i0, dst + half + i0);
+            else rotate_store_smem<T, VEC, BWD>(a, b, cc, ok, dst + i0, dst + half + i0);
           }
         }
       }
@@ -435,14 +501,19 @@ gbln_status rope_typed(const RopeArgs<T>& A, cudaStream_t s) {
     const size_t smem = (size_t)kRopeStages * geo.stage;
     const int hpl = 256 / nu < HT ? 256 / nu : HT;
     const int threads = 32 + ((nu * hpl + 31) / 32) * 32;
-    auto kern = rope_staged_kernel<T, BWD, IL>;
+    // Threads with several head rows per token keep the token's cos/sin in
+    // registers; with one row per token they read it as they go.
+    auto kern = HT > hpl ? rope_staged_kernel<T, BWD, IL, true> : rope_staged_kernel<T, BWD, IL, false>;
     static std::atomic<uint64_t> attr_done{0};  // one bit per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return GBLN_ERR_CUDA; }
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)(kRopeStages * (kStageTarget + 1024))) != cudaSuccess) {
+      const int cap = (int)(kRopeStages * (kStageTarget + 1024));
+      if (cudaFuncSetAttribute(rope_staged_kernel<T, BWD, IL, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, cap) != cudaSuccess ||
+          cudaFuncSetAttribute(rope_staged_kernel<T, BWD, IL, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, cap) != cudaSuccess) {
         cudaGetLastError();
         return GBLN_ERR_CUDA;
       }
