@@ -685,7 +685,8 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+            # arithmetic type of the kernels (float32 everywhere); io_dtype is what they read and write
+            "dtype": "f32", "io_dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32", "data": "synthetic",
             "config": config,
             "achieved_hbm_gbs_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
             "frac_of_peak_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9 / peak, 4),
