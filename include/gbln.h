@@ -79,14 +79,25 @@ const char* gbln_status_string(int status);
 int gbln_version(void);
 
 /*
- * Per-device error word of the current device.  Kernels that wait on their own
- * asynchronous (TMA bulk) copies bound every wait; if a bound is ever exceeded
- * the kernel ORs bit 1 (wait timeout) into this word and stops early instead of
- * hanging, so its outputs are then incomplete.  *code receives the word; clear
- * != 0 resets it to zero.  Synchronous (device-wide copy): call it outside hot
- * loops.  Errors: INVALID_ARG for a null code, CUDA if the device is unreachable.
+ * Per-device error word of the current device, a set of bits:
+ *   1  a kernel's bounded wait on its own asynchronous (TMA bulk) copies ran
+ *      out; the kernel stopped early instead of hanging, so its outputs are
+ *      incomplete;
+ *   2  a RoPE call met a position outside [0, max_pos); that token's outputs
+ *      are NaN (the table is not read).
+ * *code receives the word; clear != 0 resets it to zero.  Synchronous
+ * (device-wide copy): call it outside hot loops.  Errors: INVALID_ARG for a
+ * null code, CUDA if the device is unreachable.
  */
 gbln_status gbln_device_error(uint32_t* code, int clear);
+
+/*
+ * Self-test of the timeout path: launches one thread that waits, with the
+ * bounded poll loop of the TMA pipelines, on a barrier nothing completes; after
+ * `polls` polls (1 <= polls <= 2^22) it sets bit 1 of the device error word and
+ * returns.  Touches no caller memory; the context stays usable.  For tests.
+ */
+gbln_status gbln_selftest_wait_timeout(uint32_t polls, gbln_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* RMSNorm with fused residual add ([FL] Transformer Block 结构, 训练配置示例;  */

@@ -44,6 +44,7 @@ _SIGNATURES = {
     "gbln_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gbln_version": (ctypes.c_int, []),
     "gbln_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
+    "gbln_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _vp]),
     "gbln_rmsnorm_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, ctypes.c_int, ctypes.c_int, _vp]),
     "gbln_rmsnorm_bwd_num_partials": (_i64, [_i64, _i64, ctypes.c_int]),
     "gbln_rmsnorm_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]),
@@ -110,11 +111,22 @@ def version() -> int:
     return library().gbln_version()
 
 
+ERR_WAIT_TIMEOUT = 1   # bits of the device error word
+ERR_BAD_POSITION = 2
+
+
 def device_error(clear: bool = False) -> int:
-    """``gbln_device_error``: the current device's error word (0 = no kernel gave up a wait)."""
+    """``gbln_device_error``: the current device's error word (0 = nothing reported;
+    ERR_WAIT_TIMEOUT, ERR_BAD_POSITION)."""
     v = ctypes.c_uint32(0)
     _check("gbln_device_error", library().gbln_device_error(ctypes.byref(v), 1 if clear else 0))
     return int(v.value)
+
+
+def selftest_wait_timeout(polls: int = 1024) -> None:
+    """``gbln_selftest_wait_timeout`` on the current stream."""
+    _check("gbln_selftest_wait_timeout",
+           library().gbln_selftest_wait_timeout(int(polls), torch.cuda.current_stream().cuda_stream))
 
 
 def _check(fn, status):

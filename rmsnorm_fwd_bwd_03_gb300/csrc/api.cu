@@ -64,7 +64,7 @@ extern "C" const char* gbln_status_string(int status) {
   }
 }
 
-extern "C" int gbln_version(void) { return 100; }
+extern "C" int gbln_version(void) { return 10100; }
 
 extern "C" gbln_status gbln_device_error(uint32_t* code, int clear) {
   if (!code) return GBLN_ERR_INVALID_ARG;
@@ -84,4 +84,27 @@ extern "C" gbln_status gbln_device_error(uint32_t* code, int clear) {
     }
   }
   return GBLN_OK;
+}
+
+namespace gbln {
+namespace {
+// One thread waits, with the same bounded poll loop the TMA pipelines use, on an
+// mbarrier that nothing will ever complete; when the bound runs out it reports
+// a wait timeout exactly as a pipeline would and returns.
+__global__ void wait_timeout_kernel(uint32_t polls, unsigned int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  mbar_init_fence();
+  if (!mbar_wait(&bar, 0u, polls)) atomicOr(err, kErrWaitTimeout);
+}
+}  // namespace
+}  // namespace gbln
+
+extern "C" gbln_status gbln_selftest_wait_timeout(uint32_t polls, gbln_stream_t stream) {
+  if (polls == 0 || polls > gbln::kWaitPolls) return GBLN_ERR_INVALID_ARG;
+  unsigned int* err = gbln::device_error_word();
+  if (!err) return GBLN_ERR_CUDA;
+  gbln::wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(polls, err);
+  return cudaGetLastError() == cudaSuccess ? GBLN_OK : GBLN_ERR_CUDA;
 }

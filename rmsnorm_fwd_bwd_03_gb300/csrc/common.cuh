@@ -353,7 +353,8 @@ __device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
 // microseconds; this bound is far beyond any legitimate wait).
 constexpr uint32_t kWaitPolls = 1u << 22;
 // Bits of the per-device error word (see gbln_device_error).
-constexpr uint32_t kErrWaitTimeout = 1u;
+constexpr uint32_t kErrWaitTimeout = 1u;   // a bounded wait on an mbarrier ran out
+constexpr uint32_t kErrBadPosition = 2u;   // a RoPE position outside [0, max_pos)
 
 // ---------------------------------------------------------------------------
 // Host side

@@ -192,6 +192,7 @@ struct RopeArgs {
   int64_t max_pos, rows;
   int Hq, Hk, D;
   int64_t ldq, ldk, ldqo, ldko;
+  unsigned int* err;  // device error word: kErrBadPosition for an out-of-range position
   __device__ __forceinline__ const T* src(int64_t t, int h) const {
     return h < Hq ? q + t * ldq + (int64_t)h * D : k + t * ldk + (int64_t)(h - Hq) * D;
   }
@@ -241,8 +242,10 @@ rope_kernel(const RopeArgs<T> A, int HP) {
       for (int u = 0; u < UT; ++u) {
         const int64_t t = tb + u;
         if (t >= A.rows) break;
-        // out-of-range position: the table is not read and the outputs are NaN
+        // out-of-range position: the table is not read, the outputs are NaN and
+        // the device error word records it
         const bool ok = p[u] >= 0 && (int64_t)p[u] < A.max_pos;
+        if (!ok && threadIdx.x == 0 && h0 == hl) atomicOr(A.err, kErrBadPosition);
         const CsUnit<NP> cs = load_cs<NP, false>(A.cs + (ok ? (size_t)p[u] * half : 0) + c0, ok);
 #pragma unroll
         for (int j = 0; j < HPT; ++j) {
@@ -343,6 +346,7 @@ rope_staged_kernel(const RopeArgs<T> A, int TT, int HPL, unsigned int* err) {
       for (int tok = 0; tok < ntok; ++tok) {
         const int p = __ldg(A.pos + t0 + tok);
         const bool ok = p >= 0 && (int64_t)p < A.max_pos;
+        if (!ok) atomicOr(err, kErrBadPosition);
         spos[tok] = ok ? p : -1;
         if (ok) bytes += (uint32_t)g.csrow;
       }
@@ -484,6 +488,7 @@ gbln_status rope_typed(const RopeArgs<T>& A, cudaStream_t s) {
                    aligned16(A.cs) && (A.Hk == 0 || (aligned16(A.k) && aligned16(A.ko)));
   const int sms = sm_count();
   if (sms <= 0) return GBLN_ERR_CUDA;
+  if (!A.err) return GBLN_ERR_CUDA;
   // elements per unit: VEC on the vector path; on the element-wise path 1
   // (rotate-half) or one pair (interleaved)
   const int unit = vec ? VEC : (IL ? 2 : 1);
@@ -494,8 +499,7 @@ gbln_status rope_typed(const RopeArgs<T>& A, cudaStream_t s) {
   // tile is completely in shared memory before any of its outputs is stored.
   const size_t tok_bytes = (size_t)HT * D * sizeof(T) + (size_t)half * sizeof(float2);
   if (vec && nu <= 256 && tok_bytes <= kStageTarget) {
-    unsigned int* err = device_error_word();
-    if (!err) return GBLN_ERR_CUDA;
+    unsigned int* err = A.err;
     const int TT = (int)(kStageTarget / tok_bytes);
     const StageGeom geo = stage_geom<T>(A.Hq, A.Hk, D, TT);
     const size_t smem = (size_t)kRopeStages * geo.stage;
@@ -566,7 +570,7 @@ gbln_status rope_entry(const void* q, const void* k, void* qo, void* ko, const i
   const bool il = pairing == GBLN_ROPE_INTERLEAVED;
 #define GBLN_ROPE_ARGS(TY)                                                                     \
   RopeArgs<TY> A{(const TY*)q, (const TY*)k, (TY*)qo, (TY*)ko, pos, (const float2*)cs, max_pos, \
-                 T, Hq, Hk, D, ldq, Hk > 0 ? ldk : 0, ldqo, Hk > 0 ? ldko : 0}
+                 T, Hq, Hk, D, ldq, Hk > 0 ? ldk : 0, ldqo, Hk > 0 ? ldko : 0, device_error_word()}
   if (io == GBLN_F32) {
     GBLN_ROPE_ARGS(float);
     return il ? rope_typed<float, BWD, true>(A, s) : rope_typed<float, BWD, false>(A, s);

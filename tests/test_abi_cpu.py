@@ -215,6 +215,11 @@ def test_device_error_rejects_null(lib):
     assert lib.gbln_device_error(None, 0) == INVALID
 
 
+def test_selftest_rejects_bad_poll_counts(lib):
+    assert lib.gbln_selftest_wait_timeout(0, None) == INVALID
+    assert lib.gbln_selftest_wait_timeout((1 << 22) + 1, None) == INVALID
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     import rmsnorm_fwd_bwd_03_gb300 as gb

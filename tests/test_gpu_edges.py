@@ -259,6 +259,7 @@ def test_rope_in_place_identity_and_out_of_range(io):
     gb.rope_fwd(q, k, zeros, table, q_out=q, k_out=k)  # in place, position 0
     torch.cuda.synchronize()
     assert torch.equal(q, q0) and torch.equal(k, k0)
+    assert gb.device_error() == 0
     pos = torch.as_tensor([0, 5, 99, 100, -1, 3, 2000, 7], dtype=torch.int32, device="cuda")
     qo, ko = gb.rope_fwd(q, k, pos, table)
     torch.cuda.synchronize()
@@ -267,6 +268,15 @@ def test_rope_in_place_identity_and_out_of_range(io):
     assert torch.isnan(qo[bad].float()).all() and torch.isnan(ko[bad].float()).all()
     p = pos.cpu().numpy()[good]
     check_io(to64(qo[good]), oracle.rope_fwd(to64(q0[good]), p, 1e6), io, "q' valid rows")
+    # the out-of-range positions are reported through the device error word
+    assert gb.device_error(clear=True) == gb.ERR_BAD_POSITION
+    assert gb.device_error() == 0
+    # the register path (unaligned rows) reports them too
+    qu = _randn((T * Hq * D + 1,), dt, 63)[1:].view(T, Hq, D)
+    qo2, _ = gb.rope_fwd(qu, None, pos, table)
+    torch.cuda.synchronize()
+    assert torch.isnan(qo2[bad].float()).all()
+    assert gb.device_error(clear=True) == gb.ERR_BAD_POSITION
 
 
 # ---------------------------------------------------------------------------
@@ -334,6 +344,26 @@ def test_swiglu_guard_bands():
     gb.swiglu_bwd(d, g, u, dgate=gdg.tensor, dup=gdu.tensor)
     torch.cuda.synchronize()
     assert go.intact() and gdg.intact() and gdu.intact()
+
+
+def test_wait_timeout_is_reported_and_the_context_stays_usable():
+    # A bounded wait that nothing will satisfy runs out (no fault, no hang): the
+    # error word gets the timeout bit, and the next calls run normally.
+    assert gb.device_error() == 0
+    gb.selftest_wait_timeout(256)
+    torch.cuda.synchronize()
+    assert gb.device_error() == gb.ERR_WAIT_TIMEOUT
+    assert gb.device_error(clear=True) == gb.ERR_WAIT_TIMEOUT
+    assert gb.device_error() == 0
+    T, Hq, Hk, D = 64, 16, 8, 128
+    q = _randn((T, Hq, D), torch.bfloat16, 95)
+    k = _randn((T, Hk, D), torch.bfloat16, 96)
+    pos = torch.arange(T, dtype=torch.int32, device="cuda")
+    table = gb.rope_table(T, D, 1e6)
+    qo, ko = gb.rope_fwd(q, k, pos, table)
+    torch.cuda.synchronize()
+    assert gb.device_error() == 0
+    check_io(to64(qo), oracle.rope_fwd(to64(q), pos.cpu().numpy(), 1e6), "bf16", "q' after timeout")
 
 
 def test_device_error_word_is_clear_after_staged_kernels():

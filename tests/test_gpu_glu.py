@@ -2,7 +2,6 @@
 and erf form, ReLU), in contiguous, packed-[T, 2I] and unaligned layouts, and
 for the plain activations.  Tolerances are those of ``_checks``."""
 
-import numpy as np
 import pytest
 import torch
 

@@ -10,7 +10,6 @@ This file sorts last so that a run that stops at the first failure has already
 run every other test; it also passes alone in a fresh process.
 """
 
-import numpy as np
 import pytest
 import torch
 
