@@ -51,7 +51,7 @@ NCU_TRAFFIC = {
     # glu_bwd_vec at Qwen3-0.6B widths, full size: dram__bytes_read.sum + dram__bytes_write.sum,
     # mean of 12 launches of one one-pass ncu capture (cold L2: ~59 MB of the writes
     # are still in L2 when a launch ends)
-    ("qwen3_0p6b", "swiglu_bwd"): {"bytes": 302011861 + 142197205, "src_sha": "024e4d29115c48c2"},
+    ("qwen3_0p6b", "swiglu_bwd"): {"bytes": 302015957 + 142399403, "src_sha": "6bfac412e59e78ef"},
 }
 
 
