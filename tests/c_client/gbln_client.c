@@ -1,9 +1,10 @@
 /*
  * A plain C user of libgbln: allocates device memory with the CUDA runtime,
- * runs RMSNorm forward + backward (+ dW finalize), RoPE forward + backward and
- * SwiGLU forward + backward through the C ABI on one stream, and writes every
- * input and output (float32) to a binary file that the test compares with the
- * CPU oracle.  Inputs come from a fixed linear congruential generator.
+ * runs RMSNorm forward + backward (+ dW finalize), RoPE forward + backward,
+ * SwiGLU forward + backward, LayerNorm forward + backward (+ dW/dB finalize)
+ * and the MXFP8 RMSNorm forward through the C ABI on one stream, and writes
+ * every input and output (as float32) to a binary file that the test compares
+ * with the CPU oracle.  Inputs come from a fixed linear congruential generator.
  *
  * usage: gbln_client OUT.bin
  * exit status: 0 on success, 2 on a CUDA error, 3 on a library error.
@@ -114,6 +115,21 @@ int main(int argc, char** argv) {
   float *so = dev_alloc(T * I), *sdg = dev_alloc(T * I), *sdu = dev_alloc(T * I);
   GK(gbln_swiglu_fwd(dg, du, so, T, I, GBLN_F32, s));
   GK(gbln_swiglu_bwd(ddo, dg, du, sdg, sdu, T, I, GBLN_F32, s));
+  /* LayerNorm (residual + bias) on the same rows, and the MXFP8 RMSNorm forward */
+  float *bias = host_rand(H, 1.f, 0.f), *dbias = dev_from(bias, H);
+  float *ly = dev_alloc(T * H), *lh = dev_alloc(T * H), *lmean = dev_alloc(T), *lrstd = dev_alloc(T);
+  float *ldx = dev_alloc(T * H);
+  GK(gbln_layernorm_fwd(dx_, dr_, dw_, dbias, ly, lh, lmean, lrstd, T, H, eps, GBLN_F32, GBLN_F32, s));
+  int64_t LP = gbln_layernorm_bwd_num_partials(T, H, GBLN_F32);
+  if (LP < 1) return 3;
+  float *lpart = dev_alloc((size_t)LP * 2 * H), *ldW = dev_alloc(H), *ldB = dev_alloc(H);
+  GK(gbln_layernorm_bwd(ddy, ddres, lh, dw_, lmean, lrstd, ldx, lpart, LP, T, H, GBLN_F32, GBLN_F32, s));
+  GK(gbln_layernorm_dwdb_finalize(lpart, LP, H, ldW, ldB, 0, s));
+  uint8_t *q8 = NULL, *sc8 = NULL;
+  float *mh = dev_alloc(T * H), *mrstd = dev_alloc(T);
+  CK(cudaMalloc((void**)&q8, T * H));
+  CK(cudaMalloc((void**)&sc8, T * (H / 32)));
+  GK(gbln_rmsnorm_fwd_mxfp8(dx_, dr_, dw_, NULL, q8, sc8, mh, mrstd, T, H, eps, GBLN_F32, GBLN_F32, s));
   CK(cudaStreamSynchronize(stream));
 
   uint32_t err = 0;
@@ -131,6 +147,19 @@ int main(int argc, char** argv) {
   dump(f, "dq_in", qb, T * HQ * D, 1); dump(f, "dk_in", kb, T * HK * D, 1);
   dump(f, "gate", gate, T * I, 0); dump(f, "up", up, T * I, 0); dump(f, "dout", dout, T * I, 0);
   dump(f, "out", so, T * I, 1); dump(f, "dgate", sdg, T * I, 1); dump(f, "dup", sdu, T * I, 1);
+  dump(f, "bias", bias, H, 0);
+  dump(f, "ln_y", ly, T * H, 1); dump(f, "ln_mean", lmean, T, 1); dump(f, "ln_rstd", lrstd, T, 1);
+  dump(f, "ln_dx", ldx, T * H, 1); dump(f, "ln_dW", ldW, H, 1); dump(f, "ln_dB", ldB, H, 1);
+  {
+    uint8_t hq[T * H], hs[T * (H / 32)];
+    float fq[T * H], fs[T * (H / 32)];
+    CK(cudaMemcpy(hq, q8, sizeof(hq), cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(hs, sc8, sizeof(hs), cudaMemcpyDeviceToHost));
+    for (int i = 0; i < T * H; ++i) fq[i] = (float)hq[i];
+    for (int i = 0; i < T * (H / 32); ++i) fs[i] = (float)hs[i];
+    dump(f, "y_e4m3", fq, T * H, 0);
+    dump(f, "y_scale", fs, T * (H / 32), 0);
+  }
   {
     int32_t hp[T];
     float fp[T];

@@ -13,7 +13,7 @@ import pytest
 
 import oracle
 
-from _checks import check_dw, check_io, check_rstd, dx_scale
+from _checks import check_mxfp8, check_dw, check_io, check_rstd, dx_scale
 
 pytestmark = pytest.mark.gpu
 
@@ -80,3 +80,17 @@ def test_c_client_against_oracle(tmp_path):
     dg_ref, du_ref = oracle.swiglu_bwd(do, g, u)
     check_io(d["dgate"], dg_ref, "f32", "dgate")
     check_io(d["dup"], du_ref, "f32", "dup")
+    # LayerNorm with residual and bias, backward with dres
+    ly_ref, lh_ref, lmean_ref, lrstd_ref = oracle.layernorm_fwd(x, res, w, d["bias"], 1e-5, io="f32")
+    check_io(d["ln_y"].reshape(T, H), ly_ref, "f32", "ln y")
+    check_rstd(d["ln_rstd"], lrstd_ref, "ln rstd")
+    assert np.allclose(d["ln_mean"], lmean_ref, rtol=1e-5, atol=1e-6 * np.max(np.abs(lh_ref)))
+    ldx_ref, ldw_ref, ldb_ref = oracle.layernorm_bwd(dy, dres, lh_ref, w, 1e-5)
+    check_io(d["ln_dx"].reshape(T, H), ldx_ref, "f32", "ln dx", scale=3 * dx_scale(dy, w, lrstd_ref, dres))
+    check_dw(d["ln_dW"], ldw_ref, "ln dW")
+    check_dw(d["ln_dB"], ldb_ref, "ln dB")
+    # MXFP8 RMSNorm forward: codes and scales of y
+    import torch
+    q8 = torch.from_numpy(d["y_e4m3"].astype(np.uint8).reshape(T, H))
+    sc8 = torch.from_numpy(d["y_scale"].astype(np.uint8).reshape(T, H // 32))
+    check_mxfp8(q8, sc8, y_ref, "c client y mxfp8")
