@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -51,17 +52,21 @@ NCU_TRAFFIC = {
     # glu_bwd_vec at Qwen3-0.6B widths, full size: dram__bytes_read.sum + dram__bytes_write.sum,
     # mean of 12 launches of one one-pass ncu capture (cold L2: ~59 MB of the writes
     # are still in L2 when a launch ends)
-    ("qwen3_0p6b", "swiglu_bwd"): {"bytes": 302015957 + 142399403, "src_sha": "6bfac412e59e78ef"},
+    ("qwen3_0p6b", "swiglu_bwd"): {"bytes": 302015957 + 142399403, "src_sha": "aecf78516bed526b"},
 }
 
 
 def _src_sha(op):
-    """Hash of the op's source file and the shared header it includes: the DRAM
-    traffic recorded for a kernel is reported only while both are unchanged."""
+    """Hash of the code (comments and whitespace removed) of the op's source file
+    and the shared header it includes: the DRAM traffic recorded for a kernel is
+    reported only while that code is unchanged."""
     h = hashlib.sha256()
     for name in (KERNEL_SOURCE[op], "common.cuh"):
-        with open(os.path.join(ROOT, "rmsnorm_fwd_bwd_03_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "rmsnorm_fwd_bwd_03_gb300", "csrc", name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                  # line comments
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,6 +1,9 @@
-// Shared device helpers of libgbln: 128-bit packs of bf16 / f32, fp32 row
-// reductions and host-side argument checks.  Nothing here is used by the CPU
-// oracle, and nothing from it is used here.
+// Shared device helpers of libgbln: 128-bit loads / stores and packs of bf16 /
+// f32, fp32 row reductions (warp shuffles, named barriers, compensated sums),
+// the fixed-order column sum that finishes the weight gradients, the MXFP8
+// quantisation epilogue, TMA bulk copies with bounded mbarrier waits, and the
+// host-side argument checks.  Nothing here is used by the CPU oracle, and
+// nothing from it is used here.
 #pragma once
 
 #include <cuda_runtime.h>
