@@ -26,6 +26,10 @@
  *  - Streams: work is enqueued on `stream` (NULL = the legacy default stream) and
  *    the call returns without synchronising.  Errors raised by the kernels
  *    themselves appear on the stream, not in the returned status.
+ *  - CUDA graphs: every call can be captured.  The first call of an entry point
+ *    on a device does one-time set-up (SM count, the device error word's
+ *    address, kernel shared-memory limits); make that first call outside
+ *    stream capture.
  *  - Types: `io` is the element type of activations and gradients, `wt` the type
  *    of the RMSNorm weight.  Supported: io = wt = F32; io = wt = BF16;
  *    io = BF16 with wt = F32.  Arithmetic is float32; bf16 results are rounded
