@@ -346,6 +346,68 @@ def test_swiglu_guard_bands():
     assert go.intact() and gdg.intact() and gdu.intact()
 
 
+@pytest.mark.parametrize("Hq,Hk,D,offset", [(16, 8, 128, 0), (32, 8, 128, 0), (3, 1, 130, 1)])
+def test_rope_guard_bands(Hq, Hk, D, offset):
+    # staged path (one and several rows per thread and token) and the register path
+    T, dt = 23, torch.bfloat16
+    q = _randn((T, Hq, D), dt, 85, offset=offset)
+    k = _randn((T, Hk, D), dt, 86, offset=offset)
+    pos = torch.arange(T, dtype=torch.int32, device="cuda")
+    table = gb.rope_table(T, D, 1e6)
+    gq, gk = Guarded((T, Hq, D), dt), Guarded((T, Hk, D), dt)
+    gb.rope_fwd(q, k, pos, table, q_out=gq.tensor, k_out=gk.tensor)
+    gdq, gdk = Guarded((T, Hq, D), dt), Guarded((T, Hk, D), dt)
+    gb.rope_bwd(q, k, pos, table, dq_in=gdq.tensor, dk_in=gdk.tensor)
+    torch.cuda.synchronize()
+    assert gq.intact() and gk.intact() and gdq.intact() and gdk.intact()
+    check_io(to64(gq.tensor), oracle.rope_fwd(to64(q), pos.cpu().numpy(), 1e6), "bf16", "q' guarded")
+
+
+def test_layernorm_and_mxfp8_guard_bands():
+    T, H, dt = 21, 1024, torch.bfloat16
+    x, r, dy = _randn((T, H), dt, 87), _randn((T, H), dt, 88), _randn((T, H), dt, 89)
+    w = (1 + 0.1 * _randn((H,), torch.float32, 90)).to(dt)
+    gy, gh, gdx = Guarded((T, H), dt), Guarded((T, H), dt), Guarded((T, H), dt)
+    gm, gr = Guarded((T,), torch.float32), Guarded((T,), torch.float32)
+    y, h, mean, rstd = gb.layernorm_fwd(x, w, 1e-5, r, None, y=gy.tensor, residual_out=gh.tensor,
+                                        mean=gm.tensor, rstd=gr.tensor)
+    dx, part, P = gb.layernorm_bwd(dy, h, w, mean, rstd, None, dx=gdx.tensor)
+    lib = gb.library()
+    gq, gs = Guarded((T, H), torch.uint8), Guarded((T, H // 32), torch.uint8)
+    gh2, gr2 = Guarded((T, H), dt), Guarded((T,), torch.float32)
+    st = lib.gbln_rmsnorm_fwd_mxfp8(x.data_ptr(), r.data_ptr(), w.data_ptr(), None, gq.tensor.data_ptr(),
+                                    gs.tensor.data_ptr(), gh2.tensor.data_ptr(), gr2.tensor.data_ptr(), T, H,
+                                    1e-5, gb.BF16, gb.BF16, torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    for g in (gy, gh, gdx, gm, gr, gq, gs, gh2, gr2):
+        assert g.intact()
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_rope_out_of_range_with_cos_sin_in_registers(io):
+    # 40 head rows per token: staged threads rotate several rows per token and
+    # hold the token's cos/sin in registers; a bad position must still give NaN
+    # rows and the error bit, and the other tokens the exact rotation.
+    dt = IO[io]
+    T, Hq, Hk, D = 9, 32, 8, 128
+    q = _randn((T, Hq, D), dt, 71)
+    k = _randn((T, Hk, D), dt, 72)
+    table = gb.rope_table(50, D, 1e6)
+    pos = torch.as_tensor([0, 49, 50, 7, -3, 1, 2, 3, 4], dtype=torch.int32, device="cuda")
+    assert gb.device_error() == 0
+    qo, ko = gb.rope_fwd(q, k, pos, table)
+    dq, dk = gb.rope_bwd(q, k, pos, table)
+    torch.cuda.synchronize()
+    bad, good = [2, 4], [0, 1, 3, 5, 6, 7, 8]
+    for t in (qo, ko, dq, dk):
+        assert torch.isnan(t[bad].float()).all()
+    p = pos.cpu().numpy()[good]
+    check_io(to64(qo[good]), oracle.rope_fwd(to64(q[good]), p, 1e6), io, "q' valid rows")
+    check_io(to64(dk[good]), oracle.rope_bwd(to64(k[good]), p, 1e6), io, "dk valid rows")
+    assert gb.device_error(clear=True) == gb.ERR_BAD_POSITION
+
+
 def test_wait_timeout_is_reported_and_the_context_stays_usable():
     # A bounded wait that nothing will satisfy runs out (no fault, no hang): the
     # error word gets the timeout bit, and the next calls run normally.
