@@ -12,7 +12,9 @@
 // capacity of the GPU.  Contiguous tensors are walked as one flat index space;
 // row-strided ones (gate and up as the two halves of a packed [T, 2I]
 // projection output, for instance) by (row group, column block) units.  The
-// activation is recomputed in the backward pass; nothing is saved.
+// activation is recomputed in the backward pass; nothing is saved.  The gated
+// forward can also deliver its output as MXFP8 (E4M3 codes and one E8M0 scale
+// per 32 values of a row) for the down projection.
 
 #include "common.cuh"
 

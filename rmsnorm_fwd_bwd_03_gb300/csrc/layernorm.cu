@@ -9,9 +9,11 @@
 // 128-bit loads into registers; the mean and then the variance of the centred
 // values are reduced in fp32 from registers (two passes over registers, one
 // over HBM); the weight and bias gradients are accumulated per thread for
-// fixed columns over a contiguous chunk of rows, reduced across the block's row
-// groups in a fixed order and written as one [dW | dB] partial row per block;
-// a second launch sums the partial rows in a fixed order (bitwise reproducible).
+// fixed columns over a contiguous chunk of rows (in registers for rows of up
+// to 64 vectors, otherwise in shared-memory slots so that 1024 threads stay
+// resident per SM), reduced across the block's row groups in a fixed order and
+// written as one [dW | dB] partial row per block; a second launch sums the
+// partial rows in a fixed order (bitwise reproducible).
 
 #include <atomic>
 

@@ -7,11 +7,13 @@
 //
 // HBM-bound design: each row is read once with 128-bit loads into registers,
 // reduced in fp32 with warp shuffles (plus shared memory across warps for wide
-// rows), and written once.  The weight gradient is accumulated per thread in
-// registers over a contiguous chunk of rows, reduced across the block's row
+// rows), and written once.  The weight gradient is accumulated per thread over
+// a contiguous chunk of rows (in registers, or for rows of 65..128 vectors in
+// shared-memory slots of 64-thread row groups), reduced across the block's row
 // groups in a fixed order and written as one partial row per block; a second
 // launch sums the partial rows in a fixed order.  No atomics: bitwise
-// reproducible for a fixed shape and SM count.
+// reproducible for a fixed shape and SM count.  The forward can also deliver y
+// as MXFP8 (E4M3 codes and one E8M0 scale per 32 values) for the next GEMM.
 
 #include <atomic>
 
