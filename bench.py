@@ -52,7 +52,7 @@ NCU_TRAFFIC = {
     # glu_bwd_vec at Qwen3-0.6B widths, full size: dram__bytes_read.sum + dram__bytes_write.sum,
     # mean of 12 launches of one one-pass ncu capture (cold L2: ~59 MB of the writes
     # are still in L2 when a launch ends)
-    ("qwen3_0p6b", "swiglu_bwd"): {"bytes": 302015957 + 142399403, "src_sha": "aecf78516bed526b"},
+    ("qwen3_0p6b", "swiglu_bwd"): {"bytes": 302011008 + 142262528, "src_sha": "3ff2bc8ec94f69ba"},
 }
 
 

@@ -190,19 +190,21 @@ glu_bwd_vec(const T* dout, const T* gate, const T* up, T* dgate, T* dup, int64_t
 
 // ---------------------------------------------------------------------------
 // Row-strided tensors.  A unit is (group of UNROLL consecutive rows, block of
-// kGluBlock column vectors); thread t takes column vector cb * kGluBlock + t of
-// each row of the group, so a warp's accesses stay contiguous within a row.
+// blockDim.x column vectors); thread t takes column vector j * blockDim.x + t
+// of each row of the group, so a warp's accesses stay contiguous within a row.
+// The host picks the block width so that the column blocks tile the row.
 // VEC = 1 is the element-wise path (unaligned pointers or strides).
 // ---------------------------------------------------------------------------
 template <typename T, int VEC, int ACT, int UNROLL>
 __global__ void __launch_bounds__(kGluBlock)
 glu_fwd_rows(const T* gate, const T* up, T* out, int64_t T_, int64_t ncol, int64_t ldg,
              int64_t ldu, int64_t ldo) {
-  const int64_t ncb = (ncol + kGluBlock - 1) / kGluBlock;
+  const int cb = blockDim.x;
+  const int64_t ncb = (ncol + cb - 1) / cb;
   const int64_t units = (T_ + UNROLL - 1) / UNROLL * ncb;
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const int64_t rg = u / ncb;
-    const int64_t c = (u - rg * ncb) * kGluBlock + threadIdx.x;
+    const int64_t c = (u - rg * ncb) * cb + threadIdx.x;
     if (c >= ncol) continue;
     const int64_t r0 = rg * UNROLL;
     Packed<T, VEC> g[UNROLL], v[UNROLL];
@@ -231,11 +233,12 @@ template <typename T, int VEC, int ACT, int UNROLL>
 __global__ void __launch_bounds__(kGluBlock)
 glu_bwd_rows(const T* dout, const T* gate, const T* up, T* dgate, T* dup, int64_t T_,
              int64_t ncol, int64_t ldd, int64_t ldg, int64_t ldu, int64_t lddg, int64_t lddu) {
-  const int64_t ncb = (ncol + kGluBlock - 1) / kGluBlock;
+  const int cb = blockDim.x;
+  const int64_t ncb = (ncol + cb - 1) / cb;
   const int64_t units = (T_ + UNROLL - 1) / UNROLL * ncb;
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const int64_t rg = u / ncb;
-    const int64_t c = (u - rg * ncb) * kGluBlock + threadIdx.x;
+    const int64_t c = (u - rg * ncb) * cb + threadIdx.x;
     if (c >= ncol) continue;
     const int64_t r0 = rg * UNROLL;
     Packed<T, VEC> d[UNROLL], g[UNROLL], v[UNROLL];
@@ -342,11 +345,12 @@ glu_fwd_mx(const T* gate, const T* up, MxOut mx, int64_t T_, int64_t ncol, int64
            int64_t ldu) {
   constexpr int LB = kMxBlock / VEC;
   const int64_t I = ncol * VEC;
-  const int64_t ncb = (ncol + kGluBlock - 1) / kGluBlock;
+  const int cb = blockDim.x;
+  const int64_t ncb = (ncol + cb - 1) / cb;
   const int64_t units = (T_ + UNROLL - 1) / UNROLL * ncb;
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const int64_t rg = u / ncb;
-    const int64_t c = (u - rg * ncb) * kGluBlock + threadIdx.x;
+    const int64_t c = (u - rg * ncb) * cb + threadIdx.x;
     const bool colok = c < ncol;
     const int64_t r0 = rg * UNROLL;
     Packed<T, VEC> g[UNROLL], v[UNROLL];
@@ -378,10 +382,27 @@ glu_fwd_mx(const T* gate, const T* up, MxOut mx, int64_t T_, int64_t ncol, int64
 // Host side
 // ---------------------------------------------------------------------------
 
-unsigned resident_grid(int64_t units) {
+unsigned resident_grid(int64_t units, int threads = kGluBlock) {
   const int sms = sm_count();
-  const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * (2048 / kGluBlock);
+  const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * (2048 / threads);
   return grid_for(units, 1, cap);
+}
+
+// Threads per block of the row-strided kernels: the multiple of 32 in
+// [128, kGluBlock] whose column blocks cover a row of ncol units with the
+// fewest idle lanes, the widest on a tie.  A bf16 row of 3072 values (384
+// vectors) gets two blocks of 192 instead of one and a half of 256.
+int col_block(int64_t ncol) {
+  int best = kGluBlock;
+  int64_t best_slots = -1;
+  for (int b = kGluBlock; b >= 128; b -= 32) {
+    const int64_t slots = (ncol + b - 1) / b * b;
+    if (best_slots < 0 || slots < best_slots) {
+      best = b;
+      best_slots = slots;
+    }
+  }
+  return best;
 }
 
 template <typename T, int ACT>
@@ -398,13 +419,15 @@ void glu_fwd_launch(const void* g, const void* u, void* o, int64_t rows, int64_t
   } else if (aligned && I % VEC == 0 && ldg % VEC == 0 && ldu % VEC == 0 && ldo % VEC == 0) {
     constexpr int U = 4;
     const int64_t ncol = I / VEC;
-    const int64_t units = (rows + U - 1) / U * ((ncol + kGluBlock - 1) / kGluBlock);
-    glu_fwd_rows<T, VEC, ACT, U><<<resident_grid(units), kGluBlock, 0, s>>>(
+    const int cb = col_block(ncol);
+    const int64_t units = (rows + U - 1) / U * ((ncol + cb - 1) / cb);
+    glu_fwd_rows<T, VEC, ACT, U><<<resident_grid(units, cb), cb, 0, s>>>(
         (const T*)g, (const T*)u, (T*)o, rows, ncol, ldg, ldu, ldo);
   } else {
     constexpr int U = 4;
-    const int64_t units = (rows + U - 1) / U * ((I + kGluBlock - 1) / kGluBlock);
-    glu_fwd_rows<T, 1, ACT, U><<<resident_grid(units), kGluBlock, 0, s>>>(
+    const int cb = col_block(I);
+    const int64_t units = (rows + U - 1) / U * ((I + cb - 1) / cb);
+    glu_fwd_rows<T, 1, ACT, U><<<resident_grid(units, cb), cb, 0, s>>>(
         (const T*)g, (const T*)u, (T*)o, rows, I, ldg, ldu, ldo);
   }
 }
@@ -418,12 +441,14 @@ void glu_fwd_mx_launch(const void* g, const void* u, MxOut mx, int64_t rows, int
                    reinterpret_cast<uintptr_t>(mx.q) % VEC == 0;  // VEC codes per lane
   if (vec) {
     const int64_t ncol = I / VEC;
-    const int64_t units = (rows + U - 1) / U * ((ncol + kGluBlock - 1) / kGluBlock);
-    glu_fwd_mx<T, VEC, ACT, U><<<resident_grid(units), kGluBlock, 0, s>>>((const T*)g, (const T*)u, mx,
+    const int cb = col_block(ncol);
+    const int64_t units = (rows + U - 1) / U * ((ncol + cb - 1) / cb);
+    glu_fwd_mx<T, VEC, ACT, U><<<resident_grid(units, cb), cb, 0, s>>>((const T*)g, (const T*)u, mx,
                                                                           rows, ncol, ldg, ldu);
   } else {
-    const int64_t units = (rows + U - 1) / U * ((I + kGluBlock - 1) / kGluBlock);
-    glu_fwd_mx<T, 1, ACT, U><<<resident_grid(units), kGluBlock, 0, s>>>((const T*)g, (const T*)u, mx,
+    const int cb = col_block(I);
+    const int64_t units = (rows + U - 1) / U * ((I + cb - 1) / cb);
+    glu_fwd_mx<T, 1, ACT, U><<<resident_grid(units, cb), cb, 0, s>>>((const T*)g, (const T*)u, mx,
                                                                         rows, I, ldg, ldu);
   }
 }
@@ -444,13 +469,15 @@ void glu_bwd_launch(const void* d, const void* g, const void* u, void* dg, void*
              lddg % VEC == 0 && lddu % VEC == 0) {
     constexpr int U = 2;
     const int64_t ncol = I / VEC;
-    const int64_t units = (rows + U - 1) / U * ((ncol + kGluBlock - 1) / kGluBlock);
-    glu_bwd_rows<T, VEC, ACT, U><<<resident_grid(units), kGluBlock, 0, s>>>(
+    const int cb = col_block(ncol);
+    const int64_t units = (rows + U - 1) / U * ((ncol + cb - 1) / cb);
+    glu_bwd_rows<T, VEC, ACT, U><<<resident_grid(units, cb), cb, 0, s>>>(
         (const T*)d, (const T*)g, (const T*)u, (T*)dg, (T*)du, rows, ncol, ldd, ldg, ldu, lddg, lddu);
   } else {
     constexpr int U = 2;
-    const int64_t units = (rows + U - 1) / U * ((I + kGluBlock - 1) / kGluBlock);
-    glu_bwd_rows<T, 1, ACT, U><<<resident_grid(units), kGluBlock, 0, s>>>(
+    const int cb = col_block(I);
+    const int64_t units = (rows + U - 1) / U * ((I + cb - 1) / cb);
+    glu_bwd_rows<T, 1, ACT, U><<<resident_grid(units, cb), cb, 0, s>>>(
         (const T*)d, (const T*)g, (const T*)u, (T*)dg, (T*)du, rows, I, ldd, ldg, ldu, lddg, lddu);
   }
 }

@@ -50,7 +50,10 @@ def test_glu_contiguous(act, io, T, I):
 
 @pytest.mark.parametrize("act", ACTS)
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("T,I", [(33, 3072), (3, 40), (129, 4864), (7, 13)])
+# Row widths chosen so the row-strided kernels run with each of their block
+# widths (bf16: 3072 -> 192 threads, 3584 -> 224, 2560 -> 160, 40 -> 128;
+# f32: 3072 and 4864 -> 256).
+@pytest.mark.parametrize("T,I", [(33, 3072), (3, 40), (129, 4864), (7, 13), (17, 3584), (11, 2560)])
 def test_glu_packed_halves(act, io, T, I):
     # gate and up are the two halves of one [T, 2I] projection output; the
     # gradient is written back into one packed [T, 2I] tensor as well.

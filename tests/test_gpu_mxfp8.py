@@ -132,7 +132,7 @@ def test_glu_fwd_mxfp8_contiguous(act, io, T, I):
 
 
 @pytest.mark.parametrize("io", ["bf16", "f32"])
-@pytest.mark.parametrize("T,I", [(33, 3072), (5, 96)])
+@pytest.mark.parametrize("T,I", [(33, 3072), (5, 96), (9, 3584), (6, 2560)])
 def test_glu_fwd_mxfp8_packed_halves(io, T, I):
     dt = IO[io]
     packed = _randn((T, 2 * I), dt, 23, 2.0)
