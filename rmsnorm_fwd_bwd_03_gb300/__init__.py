@@ -24,7 +24,8 @@ __all__ = [
     "layernorm_dwdb_finalize",
     "rope_table", "rope_fwd", "rope_bwd", "rope_fwd_ex", "rope_bwd_ex", "positions_from_cu_seqlens",
     "swiglu_fwd", "swiglu_bwd", "glu_fwd", "glu_bwd", "act_fwd", "act_bwd", "ACT",
-    "F32", "BF16",
+    "rmsnorm_fwd_mxfp8", "glu_fwd_mxfp8", "selftest_wait_timeout", "ERR_WAIT_TIMEOUT",
+    "ERR_BAD_POSITION", "PAIRING", "F32", "BF16",
 ]
 
 F32 = 0
@@ -159,6 +160,30 @@ def _stream(t: torch.Tensor):
     return torch.cuda.current_stream(t.device).cuda_stream
 
 
+# Shape and dtype checks.  The C entry points receive bare pointers and sizes, so a
+# tensor smaller than the sizes passed would be read or written out of bounds:
+# every tensor is checked against them here, before any call.
+def _like(t, ref, name, ref_name):
+    if t is not None and (tuple(t.shape) != tuple(ref.shape) or t.dtype != ref.dtype):
+        raise ValueError(f"{name} must have the shape {tuple(ref.shape)} and dtype {ref.dtype} of {ref_name}")
+
+
+def _vec(t, n, name, dtype=None):
+    if t is None:
+        return
+    if t.numel() != n:
+        raise ValueError(f"{name} must hold {n} elements, not {t.numel()}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, not {t.dtype}")
+
+
+def _rows_f32(t, H, name, min_rows=0):
+    if t is None:
+        return
+    if t.dtype != torch.float32 or t.dim() != 2 or t.shape[1] != H or t.shape[0] < min_rows:
+        raise ValueError(f"{name} must be float32 [P, {H}] with P >= {min_rows}, not {t.dtype} {tuple(t.shape)}")
+
+
 # ---------------------------------------------------------------------------
 # RMSNorm
 # ---------------------------------------------------------------------------
@@ -171,6 +196,11 @@ def rmsnorm_fwd(x, weight, eps, residual=None, *, y=None, residual_out=None, rst
     """
     H = x.shape[-1]
     T = x.numel() // H if H else 0
+    _like(residual, x, "residual", "x")
+    _like(y, x, "y", "x")
+    _like(residual_out if residual is not None else None, x, "residual_out", "x")
+    _vec(weight, H, "weight")
+    _vec(rstd, T, "rstd", torch.float32)
     if y is None:
         y = torch.empty_like(x)
     if residual is not None and residual_out is None:
@@ -193,6 +223,9 @@ def rmsnorm_fwd_mxfp8(x, weight, eps, residual=None, *, want_y=True, residual_ou
     """
     H = x.shape[-1]
     T = x.numel() // H if H else 0
+    _like(residual, x, "residual", "x")
+    _like(residual_out if residual is not None else None, x, "residual_out", "x")
+    _vec(weight, H, "weight")
     y = torch.empty_like(x) if want_y else None
     q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
     sc = torch.empty(x.shape[:-1] + (H // 32,), dtype=torch.uint8, device=x.device)
@@ -220,6 +253,12 @@ def rmsnorm_bwd(dy, h, weight, rstd, dresidual_out=None, *, dx=None, dw_partial=
     """``gbln_rmsnorm_bwd``.  Returns ``(dx, dw_partial, P)``; finish dW with :func:`rmsnorm_dw_finalize`."""
     H = dy.shape[-1]
     T = dy.numel() // H if H else 0
+    _like(h, dy, "h", "dy")
+    _like(dresidual_out, dy, "dresidual_out", "dy")
+    _like(dx, dy, "dx", "dy")
+    _vec(weight, H, "weight")
+    _vec(rstd, T, "rstd", torch.float32)
+    _rows_f32(dw_partial, H, "dw_partial")
     P = rmsnorm_bwd_num_partials(T, H, dy.dtype)
     if dx is None:
         dx = torch.empty_like(dy)
@@ -236,6 +275,8 @@ def rmsnorm_bwd(dy, h, weight, rstd, dresidual_out=None, *, dx=None, dw_partial=
 def rmsnorm_dw_finalize(dw_partial, P, dw=None, accumulate=False):
     """``gbln_rmsnorm_dw_finalize``: float32 dW [H] = fixed-order sum of the first P partial rows."""
     H = dw_partial.shape[-1]
+    _rows_f32(dw_partial, H, "dw_partial", int(P))
+    _vec(dw, H, "dw", torch.float32)
     if dw is None:
         dw = torch.empty(H, dtype=torch.float32, device=dw_partial.device)
     st = library().gbln_rmsnorm_dw_finalize(
@@ -251,6 +292,12 @@ def rmsnorm_bwd_noalloc(dy, h, weight, rstd, dresidual_out=None, *, dx=None, dw=
     that may overlap on the GPU must be serialised.  Returns ``(dx, dw)``."""
     H = dy.shape[-1]
     T = dy.numel() // H if H else 0
+    _like(h, dy, "h", "dy")
+    _like(dresidual_out, dy, "dresidual_out", "dy")
+    _like(dx, dy, "dx", "dy")
+    _vec(weight, H, "weight")
+    _vec(rstd, T, "rstd", torch.float32)
+    _vec(dw, H, "dw", torch.float32)
     if dx is None:
         dx = torch.empty_like(dy)
     if dw is None:
@@ -271,6 +318,13 @@ def layernorm_fwd(x, weight, eps, residual=None, bias=None, *, y=None, residual_
     """``gbln_layernorm_fwd``.  Returns ``(y, h, mean, rstd)`` (mean, rstd float32 [T])."""
     H = x.shape[-1]
     T = x.numel() // H if H else 0
+    _like(residual, x, "residual", "x")
+    _like(y, x, "y", "x")
+    _like(residual_out if residual is not None else None, x, "residual_out", "x")
+    _vec(weight, H, "weight")
+    _like(bias, weight, "bias", "weight")
+    _vec(mean, T, "mean", torch.float32)
+    _vec(rstd, T, "rstd", torch.float32)
     if y is None:
         y = torch.empty_like(x)
     if residual is not None and residual_out is None:
@@ -300,6 +354,13 @@ def layernorm_bwd(dy, h, weight, mean, rstd, dresidual_out=None, *, dx=None, dwd
     :func:`layernorm_dwdb_finalize`."""
     H = dy.shape[-1]
     T = dy.numel() // H if H else 0
+    _like(h, dy, "h", "dy")
+    _like(dresidual_out, dy, "dresidual_out", "dy")
+    _like(dx, dy, "dx", "dy")
+    _vec(weight, H, "weight")
+    _vec(mean, T, "mean", torch.float32)
+    _vec(rstd, T, "rstd", torch.float32)
+    _rows_f32(dwdb_partial, 2 * H, "dwdb_partial")
     P = layernorm_bwd_num_partials(T, H, dy.dtype)
     if dx is None:
         dx = torch.empty_like(dy)
@@ -316,6 +377,9 @@ def layernorm_bwd(dy, h, weight, mean, rstd, dresidual_out=None, *, dx=None, dwd
 def layernorm_dwdb_finalize(dwdb_partial, P, dw=None, db=None, accumulate=False):
     """``gbln_layernorm_dwdb_finalize``: float32 (dW [H], dB [H])."""
     H = dwdb_partial.shape[-1] // 2
+    _rows_f32(dwdb_partial, 2 * H, "dwdb_partial", int(P))
+    _vec(dw, H, "dw", torch.float32)
+    _vec(db, H, "db", torch.float32)
     if dw is None:
         dw = torch.empty(H, dtype=torch.float32, device=dwdb_partial.device)
     if db is None:
@@ -333,6 +397,7 @@ def layernorm_dwdb_finalize(dwdb_partial, P, dw=None, db=None, accumulate=False)
 
 def rope_table(max_pos: int, D: int, theta: float, device=None, out=None):
     """``gbln_rope_table``: float32 [max_pos, D/2, 2] of (cos, sin)(p * theta^(-2i/D))."""
+    _vec(out, max(int(max_pos), 0) * (int(D) // 2) * 2, "cos_sin", torch.float32)
     if out is None:
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         out = torch.empty((max_pos, D // 2, 2), dtype=torch.float32, device=dev)
@@ -341,11 +406,23 @@ def rope_table(max_pos: int, D: int, theta: float, device=None, out=None):
     return out
 
 
+def _table(cos_sin, D):
+    if cos_sin.dtype != torch.float32 or cos_sin.dim() != 3 or cos_sin.shape[1:] != (D // 2, 2):
+        raise ValueError(f"cos_sin must be float32 [max_pos, {D // 2}, 2], not {cos_sin.dtype} {tuple(cos_sin.shape)}")
+
+
 def _rope(name, q, k, positions, cos_sin, q_out, k_out):
+    if q.dim() != 3:
+        raise ValueError("q must be [T, Hq, D]")
     T, Hq, D = q.shape
     Hk = 0 if k is None else k.shape[1]
-    if k is not None and (k.shape[0] != T or k.shape[2] != D or k.dtype != q.dtype):
+    if k is not None and (k.dim() != 3 or k.shape[0] != T or k.shape[2] != D or k.dtype != q.dtype):
         raise ValueError("k must be [T, Hk, D] with q's T, D and dtype")
+    _like(q_out, q, "q_out", "q")
+    if k is not None:
+        _like(k_out, k, "k_out", "k")
+    _vec(positions, T, "positions", torch.int32)
+    _table(cos_sin, D)
     if q_out is None:
         q_out = torch.empty_like(q)
     if k is not None and k_out is None:
@@ -390,7 +467,14 @@ def _heads(t, name):
 
 def _rope_ex(name, q, k, positions, cos_sin, q_out, k_out, pairing):
     T, Hq, D, ldq = _heads(q, "q")
-    _, Hk, _, ldk = _heads(k, "k")
+    Tk, Hk, Dk, ldk = _heads(k, "k")
+    if k is not None and (Tk != T or Dk != D or k.dtype != q.dtype):
+        raise ValueError("k must be [T, Hk, D] with q's T, D and dtype")
+    for o, ref, nm in ((q_out, q, "q_out"), (k_out, k, "k_out")):
+        if o is not None and ref is not None and (tuple(o.shape) != tuple(ref.shape) or o.dtype != ref.dtype):
+            raise ValueError(f"{nm} must have the shape {tuple(ref.shape)} and dtype {ref.dtype}")
+    _vec(positions, T, "positions", torch.int32)
+    _table(cos_sin, D)
     if q_out is None:
         q_out = torch.empty((T, Hq, D), dtype=q.dtype, device=q.device)
     if k is not None and k_out is None:
@@ -422,6 +506,7 @@ def positions_from_cu_seqlens(cu_seqlens, T: int, out=None):
     """``gbln_positions_from_cu_seqlens``: int32 [T] position of each token in its document."""
     if cu_seqlens.dtype != torch.int32:
         raise TypeError("cu_seqlens must be int32")
+    _vec(out, int(T), "positions", torch.int32)
     if out is None:
         out = torch.empty(T, dtype=torch.int32, device=cu_seqlens.device)
     st = library().gbln_positions_from_cu_seqlens(
@@ -441,6 +526,7 @@ def swiglu_fwd(gate, up, out=None):
         raise ValueError("gate and up must have the same shape and dtype")
     I = gate.shape[-1]
     T = gate.numel() // I if I else 0
+    _like(out, gate, "out", "gate")
     if out is None:
         out = torch.empty_like(gate)
     st = library().gbln_swiglu_fwd(_dev(gate, "gate"), _dev(up, "up"), _dev(out, "out"), T, I,
@@ -455,6 +541,8 @@ def swiglu_bwd(dout, gate, up, dgate=None, dup=None):
         raise ValueError("dout, gate and up must have the same shape and dtype")
     I = gate.shape[-1]
     T = gate.numel() // I if I else 0
+    _like(dgate, gate, "dgate", "gate")
+    _like(dup, gate, "dup", "gate")
     if dgate is None:
         dgate = torch.empty_like(gate)
     if dup is None:
@@ -484,10 +572,10 @@ def _rows2d(t, name):
 def glu_fwd(gate, up, act="silu", out=None):
     """``gbln_glu_fwd``: f(gate) * up on [T, I] views whose rows may be strided
     (e.g. ``gate, up = packed.chunk(2, dim=-1)`` of a [T, 2I] tensor)."""
+    _like(up, gate, "up", "gate")
+    _like(out, gate, "out", "gate")
     T, I, ldg = _rows2d(gate, "gate")
     _, _, ldu = _rows2d(up, "up")
-    if up.shape != gate.shape or up.dtype != gate.dtype:
-        raise ValueError("gate and up must have the same shape and dtype")
     if out is None:
         out = torch.empty((T, I), dtype=gate.dtype, device=gate.device)
     _, _, ldo = _rows2d(out, "out")
@@ -501,10 +589,9 @@ def glu_fwd_mxfp8(gate, up, act="silu"):
     """``gbln_glu_fwd_mxfp8``: f(gate) * up delivered as MXFP8.  Returns
     ``(out_e4m3, out_scale)``: uint8 [T, I] codes and uint8 [T, I / 32] scales.
     gate and up may be strided row views (e.g. halves of a packed [T, 2I] tensor)."""
+    _like(up, gate, "up", "gate")
     T, I, ldg = _rows2d(gate, "gate")
     _, _, ldu = _rows2d(up, "up")
-    if up.shape != gate.shape or up.dtype != gate.dtype:
-        raise ValueError("gate and up must have the same shape and dtype")
     q = torch.empty((T, I), dtype=torch.uint8, device=gate.device)
     sc = torch.empty((T, I // 32), dtype=torch.uint8, device=gate.device)
     st = library().gbln_glu_fwd_mxfp8(gate.data_ptr(), up.data_ptr(), q.data_ptr(), sc.data_ptr(),
@@ -516,11 +603,13 @@ def glu_fwd_mxfp8(gate, up, act="silu"):
 def glu_bwd(dout, gate, up, act="silu", dgate=None, dup=None):
     """``gbln_glu_bwd``.  Returns ``(dgate, dup)``; pass views of one [T, 2I] tensor
     as ``dgate``/``dup`` to get the packed gradient of a fused projection."""
+    _like(up, gate, "up", "gate")
+    _like(dout, gate, "dout", "gate")
+    _like(dgate, gate, "dgate", "gate")
+    _like(dup, gate, "dup", "gate")
     T, I, ldd = _rows2d(dout, "dout")
     _, _, ldg = _rows2d(gate, "gate")
     _, _, ldu = _rows2d(up, "up")
-    if not (dout.shape == gate.shape == up.shape) or not (dout.dtype == gate.dtype == up.dtype):
-        raise ValueError("dout, gate and up must have the same shape and dtype")
     if dgate is None:
         dgate = torch.empty((T, I), dtype=gate.dtype, device=gate.device)
     if dup is None:
@@ -536,6 +625,7 @@ def glu_bwd(dout, gate, up, act="silu", dgate=None, dup=None):
 
 def act_fwd(x, act="silu", out=None):
     """``gbln_act_fwd``: f(x) elementwise on a contiguous tensor."""
+    _like(out, x, "out", "x")
     if out is None:
         out = torch.empty_like(x)
     st = library().gbln_act_fwd(_dev(x, "x"), _dev(out, "out"), x.numel(), ACT[act], _io(x), _stream(x))
@@ -545,6 +635,8 @@ def act_fwd(x, act="silu", out=None):
 
 def act_bwd(dy, x, act="silu", dx=None):
     """``gbln_act_bwd``: dy * f'(x) elementwise on contiguous tensors."""
+    _like(dy, x, "dy", "x")
+    _like(dx, x, "dx", "x")
     if dx is None:
         dx = torch.empty_like(x)
     st = library().gbln_act_bwd(_dev(dy, "dy"), _dev(x, "x"), _dev(dx, "dx"), x.numel(), ACT[act], _io(x),
