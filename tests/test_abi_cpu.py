@@ -228,3 +228,59 @@ def test_binding_refuses_cpu_tensors(lib):
         gb.rmsnorm_fwd(x, torch.ones(8), 1e-5)
     with pytest.raises(ValueError):
         gb.swiglu_fwd(x, x)
+
+
+def _cuda_include():
+    import shutil
+    for cand in ("/usr/local/cuda", os.path.dirname(os.path.dirname(shutil.which("nvcc") or "/x/x"))):
+        if os.path.exists(os.path.join(cand, "include", "cuda_runtime_api.h")):
+            return os.path.join(cand, "include")
+    return None
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c", "c11"), ("c++", "c++11"), ("c++", "c++17")])
+def test_header_compiles_cleanly(tmp_path, lang, std):
+    # The header is usable from plain C and from C++ without warnings, and with
+    # the CUDA runtime header included first (cudaStream_t and the stream handle
+    # type agree) or not at all.
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc" if lang == "c" else "g++")
+    if gcc is None:
+        pytest.skip("no host compiler")
+    cuda_inc = _cuda_include()
+    srcs = {"plain": '#include "gbln.h"\nint main(void) { return gbln_version() > 0 ? 0 : 1; }\n'}
+    if cuda_inc:
+        srcs["with_cuda"] = ('#include <cuda_runtime_api.h>\n#include "gbln.h"\n'
+                             "int main(void) { cudaStream_t s = 0; return gbln_swiglu_fwd(0, 0, 0, 0, 1, GBLN_BF16, s); }\n")
+    for tag, text in srcs.items():
+        src = tmp_path / (f"{tag}.c" if lang == "c" else f"{tag}.cpp")
+        src.write_text(text)
+        cmd = [gcc, f"-std={std}", "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only",
+               "-I", os.path.join(ROOT, "include"), str(src)]
+        if tag == "with_cuda":
+            cmd[1:1] = ["-isystem", cuda_inc]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, f"{tag} {std}: {r.stderr}"
+
+
+def test_c_client_links_against_the_library(lib, tmp_path):
+    # The plain-C client program (run against the oracle by the GPU tests) links
+    # against libgbln with every entry point it uses resolved.
+    import shutil
+    import subprocess
+    from rmsnorm_fwd_bwd_03_gb300._build import LIBDIR
+    gcc, cuda_inc = shutil.which("gcc"), _cuda_include()
+    if gcc is None or cuda_inc is None:
+        pytest.skip("no host compiler or CUDA headers")
+    cuda = os.path.dirname(cuda_inc)
+    lib64 = os.path.join(cuda, "lib64")
+    if not os.path.isdir(lib64):
+        lib64 = os.path.join(cuda, "targets", os.uname().machine + "-linux", "lib")
+    exe = tmp_path / "gbln_client"
+    cmd = [gcc, "-O1", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+           os.path.join(ROOT, "tests", "c_client", "gbln_client.c"), "-o", str(exe),
+           "-L", LIBDIR, "-lgbln", "-L", lib64, "-lcudart", "-Wl,--no-undefined"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert exe.exists()
