@@ -119,3 +119,16 @@ def test_gated_units_reject_mismatched_tensors():
         gb.act_fwd(_t(100), "silu", out=_t(99))
     with pytest.raises(ValueError, match="dy"):
         gb.act_bwd(_t(99), _t(100), "silu")
+
+
+def test_missing_library_raises_instead_of_falling_back(monkeypatch, tmp_path):
+    # There is no CPU implementation behind the binding: with the shared library
+    # absent, a call that passes its argument checks raises.
+    monkeypatch.setattr(gb, "_lib", None)
+    monkeypatch.setattr(gb, "_LIB_PATH", str(tmp_path / "libgbln.so"))
+    with pytest.raises(RuntimeError, match="libgbln.so not found"):
+        gb.library()
+    with pytest.raises(RuntimeError, match="no fallback"):
+        gb.rmsnorm_bwd_num_partials(T, H)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        gb.version()
