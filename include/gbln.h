@@ -20,8 +20,13 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Memory: every pointer is DEVICE memory on the current CUDA device, owned and
- *    allocated by the caller.  The library never allocates, never frees and keeps
- *    no state between calls other than a per-device cache of the SM count.
+ *    allocated by the caller.  The library never allocates and never frees.  Its
+ *    only state is per device: the SM count, the device error word, flags that
+ *    record which kernels' shared-memory limits have been raised, and the fixed
+ *    scratch array of gbln_rmsnorm_bwd_noalloc.  It tracks 64 devices: on a
+ *    device with ordinal 64 or above, the calls that need that state (the
+ *    backward passes, RoPE, the gated units and activations, the error word)
+ *    return GBLN_ERR_CUDA.
  *  - Layout: row-major and contiguous.  "[T, H]" means T rows of H elements.
  *  - Streams: work is enqueued on `stream` (NULL = the legacy default stream) and
  *    the call returns without synchronising.  Errors raised by the kernels
