@@ -64,10 +64,12 @@ def test_check_mxfp8_accepts_the_oracle_and_rejects_a_flipped_code_or_scale():
     y, _ = _ref((8, 128), seed=2)
     q, sc = oracle.mxfp8_quantize(y)
     check_mxfp8(torch.from_numpy(q), torch.from_numpy(sc), y, "oracle codes")
-    # one code moved by one E4M3 step: the block maximum, which lies in [256, 448] after
-    # scaling, where a step is 16 or 32 and the 1e-5 window cannot reach the next code
+    # one code moved by one E4M3 step: the block maximum, away from any rounding midpoint
+    # (asserted), so that no value within the 1e-5 window rounds to the moved code
     b = 3
     j = int(np.argmax(np.abs(y[1, 32 * b:32 * b + 32]))) + 32 * b
+    t = y[1, j] / 2.0 ** (int(sc[1, b]) - 127)
+    assert oracle.round_to_e4m3(t * (1 - 1e-5)) == oracle.round_to_e4m3(t * (1 + 1e-5))
     q2 = q.copy()
     q2[1, j] = q2[1, j] - 1 if (q2[1, j] & 0x7) else q2[1, j] + 1
     with pytest.raises(AssertionError, match="codes off"):
