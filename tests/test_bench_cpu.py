@@ -52,3 +52,16 @@ def test_reference_arm_under_torchrun_prints_once():
     lines = _lines(r.stdout)
     assert len(lines) == 1, r.stdout
     _check(lines[0], 2)
+
+
+def test_gpu_arm_refuses_to_run_without_a_gpu():
+    # The measured path has no CPU fallback: on a machine without a CUDA device the
+    # bench's own arm exits non-zero instead of timing something else.
+    import pytest
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    r = subprocess.run([sys.executable, "bench.py", "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "no CUDA device" in r.stderr and not _lines(r.stdout)
