@@ -59,6 +59,18 @@ def test_bf16_sum_rounding_matches_torch_on_bf16_pairs():
     assert np.array_equal(got, ref)
 
 
+def test_round_io_matches_torch_casts():
+    # round_io picks the I/O precision: torch's float32 and bfloat16 casts are
+    # independent round-to-nearest-even implementations; None keeps float64.
+    g = torch.Generator().manual_seed(4)
+    v = (torch.randn(50000, generator=g, dtype=torch.float64) * 10)
+    a = v.numpy()
+    assert np.array_equal(oracle.round_io(a, "f32"), v.to(torch.float32).double().numpy())
+    assert np.array_equal(oracle.round_io(a, "bf16"), v.to(torch.bfloat16).double().numpy())
+    assert np.array_equal(oracle.round_io(a, None), a)
+    assert not np.array_equal(oracle.round_io(a, "f32"), a)
+
+
 # ---------------------------------------------------------------------------
 # RMSNorm forward
 # ---------------------------------------------------------------------------
@@ -376,6 +388,18 @@ def test_activation_identities():
     assert np.allclose(dg, dg2, rtol=1e-13, atol=1e-15) and np.allclose(du, du2, rtol=1e-13, atol=1e-15)
 
 
+def test_activation_values_and_slopes_at_zero():
+    # Every activation is 0 at 0.  The slopes there: 1/2 for SiLU and both GeLU
+    # forms (sigma(0) = Phi(0) = 1/2); ReLU takes the subgradient 0.
+    z = np.array([0.0])
+    for name in ("silu", "gelu_tanh", "gelu_erf", "relu"):
+        assert oracle.act(name, z)[0] == 0.0
+    for name in ("silu", "gelu_tanh", "gelu_erf"):
+        assert oracle.act_grad(name, z)[0] == 0.5
+    assert oracle.act_grad("relu", z)[0] == 0.0
+    assert oracle.act_grad("relu", np.array([1e-300]))[0] == 1.0
+
+
 @pytest.mark.parametrize("name", ["silu", "gelu_tanh", "gelu_erf", "relu"])
 def test_activation_grad_central_differences(name):
     x = np.array([-4.1, -2.3, -0.7, -0.05, 0.13, 0.9, 1.7, 3.2, 5.5])
@@ -460,6 +484,16 @@ def test_layernorm_closed_forms():
     assert dx[0, 0] == pytest.approx(0.25, abs=1e-15) and dw[0] == 0.0 and db[0] == 1.5
 
 
+def test_layernorm_residual_rounded_before_normalising():
+    # As for RMSNorm: with bf16 I/O the stored h is the bf16 sum, and y normalises that h.
+    x = np.array([[1.0, 3.0]])
+    r = np.array([[2.0 ** -8, 0.0]])  # 1 + 2^-8 is a tie: rounds to 1
+    y, h, mean, rstd = oracle.layernorm_fwd(x, r, np.ones(2), None, 0.0, io="bf16")
+    assert np.array_equal(h, [[1.0, 3.0]])
+    assert mean[0] == 2.0 and rstd[0] == 1.0
+    assert np.array_equal(y, [[-1.0, 1.0]])
+
+
 @pytest.mark.parametrize("H", [2, 5, 8])
 def test_layernorm_bwd_central_differences(H):
     rng = np.random.default_rng(31 + H)
@@ -538,6 +572,10 @@ def test_e4m3_format_constants():
     # every finite code decodes to a value that encodes back to the same code
     codes = np.arange(256, dtype=np.uint8)[~np.isnan(vals)]
     assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_decode(codes)), codes)
+    # NaN encodes to the all-ones exponent and mantissa (0x7f), which decodes to NaN
+    with np.errstate(invalid="ignore"):  # the NaN's exponent and mantissa fields are computed, then replaced
+        nan_code = oracle.e4m3_encode(np.array([np.nan]))[0]
+    assert nan_code & 0x7F == 0x7F and np.isnan(oracle.e4m3_decode(np.array([nan_code]))[0])
 
 
 def test_e4m3_rounding_matches_torch_cast_in_range():
