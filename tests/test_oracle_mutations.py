@@ -104,6 +104,46 @@ MUTANTS = [
     ("cu_seqlens_not_differenced", "cu[1:] - cu[:-1]", "cu[1:]", ("positions",)),
     ("round_io_f32_as_bf16", '    if io == "f32":\n        return round_to_f32(a)',
      '    if io == "f32":\n        return round_to_bf16(a)', ("round_io",)),
+    ("rms_residual_ignored",
+     "    if residual is None:\n        h = x\n    else:\n        h = round_io(x + np.asarray(residual, dtype=np.float64), io)\n    ms",
+     "    h = x\n    ms", RMS),
+    ("rms_bwd_sum_not_mean", "c = np.mean(g * n, axis=-1)", "c = np.sum(g * n, axis=-1)", RMS),
+    ("rms_bwd_weight_dropped", "g = dy * w\n", "g = dy\n", RMS),
+    ("rms_dw_chunks_eps_dropped", "rstd = 1.0 / np.sqrt(np.mean(hb * hb, axis=-1) + eps)",
+     "rstd = 1.0 / np.sqrt(np.mean(hb * hb, axis=-1))", RMS),
+    ("rms_dw_chunks_skip_last_row", "for t0 in range(0, T, rows_per_chunk):",
+     "for t0 in range(0, T - 1, rows_per_chunk):", RMS),
+    ("ln_weight_dropped", "y = np.asarray(weight, dtype=np.float64) * c * rstd[..., None]",
+     "y = c * rstd[..., None]", LN),
+    ("ln_bwd_residual_grad_dropped",
+     "        dx = dx + np.asarray(dres, dtype=np.float64)\n    return dx, np.sum",
+     "        pass\n    return dx, np.sum", LN),
+    ("ln_bwd_weight_dropped", "g = dy * np.asarray(weight, dtype=np.float64)\n    dx", "g = dy\n    dx", LN),
+    ("rope_cos_from_sin", "    cos = np.cos(angle)[:, None, :]", "    cos = np.sin(angle)[:, None, :]", ROPE),
+    ("rope_second_sign", "y2 = x2 * cos + x1 * sin", "y2 = x2 * cos - x1 * sin", ROPE),
+    ("rope_half_outputs_swapped", "        out[..., :half] = y1\n        out[..., half:] = y2",
+     "        out[..., :half] = y2\n        out[..., half:] = y1", ROPE),
+    ("rope_frequency_over_half", "return np.power(float(theta), -2.0 * i / D)",
+     "return np.power(float(theta), -2.0 * i / (D // 2))", ROPE),
+    ("swiglu_bwd_s_for_one_minus_s", "dgate = dout * u * s * (1.0 + g * (1.0 - s))",
+     "dgate = dout * u * s * (1.0 + g * s)", ACTS),
+    ("gelu_tanh_half_dropped", "return 0.5 * x * (1.0 + np.tanh(", "return x * (1.0 + np.tanh(", ACTS),
+    ("gelu_tanh_root_dropped", "_SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)", "_SQRT_2_OVER_PI = 2.0 / math.pi", ACTS),
+    ("gelu_erf_density_norm", "pdf = np.exp(-0.5 * x * x) / math.sqrt(2.0 * math.pi)",
+     "pdf = np.exp(-0.5 * x * x) / math.sqrt(math.pi)", ACTS),
+    ("glu_bwd_up_dropped", "return dout * np.asarray(up, dtype=np.float64) * act_grad(name, gate)",
+     "return dout * act_grad(name, gate)", ACTS),
+    ("e4m3_one_bit_too_many", "quantum = np.ldexp(1.0, e - _E4M3_MBITS)", "quantum = np.ldexp(1.0, e - _E4M3_MBITS - 1)", MX),
+    ("e4m3_sign_lost", "np.copysign(r, a))", "r)", MX),
+    ("e4m3_encode_exponent_bias", "ef = np.where(normal, e + 7, 0)", "ef = np.where(normal, e + 8, 0)", MX),
+    ("mx_one_scale_per_tensor", "se = mx_scale_exponent(np.max(np.abs(vb), axis=-1))",
+     "se = mx_scale_exponent(np.max(np.abs(vb)) + 0 * np.max(np.abs(vb), axis=-1))", MX),
+    ("mx_scale_multiplied", "q = round_to_e4m3(vb / np.ldexp(1.0, se)[..., None])",
+     "q = round_to_e4m3(vb * np.ldexp(1.0, se)[..., None])", MX),
+    ("mx_zero_block_exponent", "-_E8M0_BIAS)\n    return np.clip", "0)\n    return np.clip", MX),
+    ("bf16_exponent_off", "np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)", "np.ldexp(np.rint(np.ldexp(m, 8)), e - 9)", ("bf16",)),
+    ("positions_of_no_documents", "        return np.zeros(0, dtype=np.int64)", "        return np.zeros(1, dtype=np.int64)",
+     ("positions",)),
 ]
 
 
