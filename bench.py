@@ -38,7 +38,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "fwd+bwd tokens/s and achieved HBM GB/s (% of GB300 peak), RMSNorm/RoPE/SwiGLU"
-DEFAULT_WORKLOAD = "qwen3_0p6b"
+DEFAULT_WORKLOAD = "llama3_8b_packed_outliers"
 FALLBACK_HBM_GBS = 6800.0
 OPS = ["positions", "rmsnorm_fwd", "rope_fwd", "swiglu_fwd", "swiglu_bwd", "rope_bwd",
        "rmsnorm_bwd", "rmsnorm_dw_finalize"]
@@ -259,8 +259,10 @@ def e2e_pipelined(wl, device, steps, warmup, world, seed):
     upload and step i-1's download; every step's copies are inside the timed
     region."""
     sets = [Step(wl, device, seed), Step(wl, device, seed)]
-    host_in = sets[0].in_arena.cpu().pin_memory()
-    host_out = [torch.empty(st.out_arena.shape, dtype=torch.uint8, pin_memory=True) for st in sets]
+    host_in = torch.empty(sets[0].in_arena.shape, dtype=torch.uint8, pin_memory=True)
+    host_in.copy_(sets[0].in_arena)
+    # one host buffer for the results: the read-backs are ordered on one stream
+    host_out = torch.empty(sets[0].out_arena.shape, dtype=torch.uint8, pin_memory=True)
     s_in, s_comp, s_out = (torch.cuda.Stream(device) for _ in range(3))
     calls = [st.calls(s_comp.cuda_stream) for st in sets]
     ev_in = [torch.cuda.Event() for _ in sets]
@@ -283,7 +285,7 @@ def e2e_pipelined(wl, device, steps, warmup, world, seed):
                 ev_comp[b].record(s_comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[b])
-                host_out[b].copy_(sets[b].out_arena, non_blocking=True)
+                host_out.copy_(sets[b].out_arena, non_blocking=True)
                 ev_out[b].record(s_out)
 
     run(warmup)
@@ -326,21 +328,44 @@ def run_calls(calls, events=None):
 # CPU oracle timing
 # ---------------------------------------------------------------------------
 
-def oracle_step(wl, inp):
-    """One fwd + bwd pass of the oracle over the rows of ``inp`` (float64 numpy arrays)."""
+# The oracle's calls in step order: (operator, fn(wl, inp, state)).  Each runs on
+# the float64 copies of a contiguous block of tokens; h comes from the forward.
+def _oracle_ops():
     import oracle
-    pos = oracle.positions_from_cu_seqlens(inp["cu_seqlens"])
-    y, h, rstd = oracle.rmsnorm_fwd(inp["x"], inp["residual"], inp["weight"], wl.eps, io=wl.io)
-    oracle.rope_fwd(inp["q"], pos, wl.theta)
-    oracle.rope_fwd(inp["k"], pos, wl.theta)
-    oracle.swiglu_fwd(inp["gate"], inp["up"])
-    oracle.swiglu_bwd(inp["dout"], inp["gate"], inp["up"])
-    oracle.rope_bwd(inp["dq"], pos, wl.theta)
-    oracle.rope_bwd(inp["dk"], pos, wl.theta)
-    oracle.rmsnorm_bwd(inp["dy"], inp["dres"], h, inp["weight"], wl.eps)
+
+    def rms_fwd(wl, inp, st):
+        st["h"] = oracle.rmsnorm_fwd(inp["x"], inp["residual"], inp["weight"], wl.eps, io=wl.io)[1]
+
+    return [
+        ("positions", lambda wl, inp, st: st.__setitem__(
+            "pos", oracle.positions_from_cu_seqlens(inp["cu_seqlens"]))),
+        ("rmsnorm_fwd", rms_fwd),
+        ("rope_fwd", lambda wl, inp, st: (oracle.rope_fwd(inp["q"], st["pos"], wl.theta),
+                                          oracle.rope_fwd(inp["k"], st["pos"], wl.theta))),
+        ("swiglu_fwd", lambda wl, inp, st: oracle.swiglu_fwd(inp["gate"], inp["up"])),
+        ("swiglu_bwd", lambda wl, inp, st: oracle.swiglu_bwd(inp["dout"], inp["gate"], inp["up"])),
+        ("rope_bwd", lambda wl, inp, st: (oracle.rope_bwd(inp["dq"], st["pos"], wl.theta),
+                                          oracle.rope_bwd(inp["dk"], st["pos"], wl.theta))),
+        # dX and the weight gradient summed over every row of the block
+        ("rmsnorm_bwd", lambda wl, inp, st: oracle.rmsnorm_bwd(inp["dy"], inp["dres"], st["h"],
+                                                               inp["weight"], wl.eps)),
+    ]
+
+
+def oracle_step(wl, inp, per_op=None):
+    """One fwd + bwd pass of the oracle over the rows of ``inp`` (float64 numpy
+    arrays); with ``per_op`` (a dict) each operator's seconds are added to it."""
+    st = {}
+    for name, fn in _oracle_ops():
+        t0 = time.perf_counter()
+        fn(wl, inp, st)
+        if per_op is not None:
+            per_op[name] = per_op.get(name, 0.0) + time.perf_counter() - t0
 
 
 def oracle_sample_inputs(wl, rows):
+    """The first ``rows`` tokens of a workload of the same widths and document law
+    (seed 0), as float64 numpy arrays: a contiguous block of consecutive tokens."""
     from rmsnorm_fwd_bwd_03_gb300.workload import make_inputs, scaled
     small = scaled(wl, rows, "_sample")
     inp = make_inputs(small, "cpu", seed=0)
@@ -353,18 +378,102 @@ def oracle_sample_inputs(wl, rows):
     return small, out
 
 
-def time_oracle(wl, rows, budget_s):
-    small, inp = oracle_sample_inputs(wl, rows)
-    n, t0 = 0, time.perf_counter()
-    while True:
+def host_cpu():
+    """CPU model and logical core count of this host (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu model")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"cpu_model": model or "unknown", "host_logical_cores": os.cpu_count()}
+
+
+class PinnedToOneCore:
+    """Restrict this process to one core of its allowed set while timing the
+    single-threaded oracle (restored afterwards)."""
+
+    def __enter__(self):
+        self.saved = None
+        self.core = None
+        if hasattr(os, "sched_setaffinity"):
+            try:
+                self.saved = os.sched_getaffinity(0)
+                self.core = min(self.saved)
+                os.sched_setaffinity(0, {self.core})
+            except OSError:
+                self.saved = None
+        return self
+
+    def cores(self):
+        return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 1
+
+    def __exit__(self, *exc):
+        if self.saved is not None:
+            os.sched_setaffinity(0, self.saved)
+
+
+ORACLE_ROWS = 4096          # contiguous tokens per oracle pass (at most)
+REFERENCE_ARM_BUDGET_S = 150.0  # the whole --impl reference run, warm-up included
+
+
+def reference_rows(wl, passes, budget_s=REFERENCE_ARM_BUDGET_S, lo=256):
+    """Tokens per reference-arm step: ORACLE_ROWS when ``passes`` passes of that many
+    fit in ``budget_s`` seconds, else fewer (a multiple of ``lo``, at least ``lo``),
+    from the measured cost of one calibration pass over ``lo`` tokens."""
+    small, inp = oracle_sample_inputs(wl, min(lo, wl.T))
+    with PinnedToOneCore():
+        t0 = time.perf_counter()
         oracle_step(small, inp)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    return {"value": n * rows / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} passes of all 8 operators over the first {rows} tokens of {wl.name} "
-                      f"(same widths), float64 numpy, single thread, {el:.1f} s"}
+        per_row = (time.perf_counter() - t0) / small.T
+    rows = int(budget_s / max(passes, 1) / max(per_row, 1e-9)) // lo * lo
+    return max(lo, min(ORACLE_ROWS, rows, wl.T))
+
+
+def time_oracle(wl, rows, budget_s, passes=None, warmup=0):
+    """The float64 oracle over a contiguous block of ``rows`` tokens of the workload,
+    pinned to one core: whole passes of all operators until ``budget_s`` seconds
+    have run (or exactly ``passes`` passes), and each operator's share.  Tokens/s
+    of the block stand for the whole workload (extrapolated: every operator is
+    independent per token, so its cost is linear in the token count)."""
+    rows = min(rows, wl.T)
+    small, inp = oracle_sample_inputs(wl, rows)
+    per_op = {}
+    with PinnedToOneCore() as pin:
+        for _ in range(warmup):
+            oracle_step(small, inp)
+        n, t0 = 0, time.perf_counter()
+        while True:
+            oracle_step(small, inp, per_op)
+            n += 1
+            el = time.perf_counter() - t0
+            if (passes is not None and n >= passes) or (passes is None and el >= budget_s):
+                break
+        cores = pin.cores()
+        core = pin.core
+    ops = {k: {"tokens_per_s": round(n * rows / v, 1), "s_per_pass": round(v / n, 4)}
+           for k, v in per_op.items()}
+    info = host_cpu()
+    label = "extrapolated" if rows < wl.T else "full workload"
+    return {"value": n * rows / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} passes of all 8 operators (forward and backward) over a contiguous block "
+                      f"of {rows} tokens of {wl.name} (same widths and document law, seed 0), float64 "
+                      f"numpy, one thread pinned to core {core}, {el:.1f} s; tokens/s {label} to the "
+                      f"{wl.T}-token workload",
+            "rows": rows, "passes": n, "seconds": round(el, 3), "tokens_per_s_label": label,
+            "pinned_core": core, **info, "per_operator": ops, "ms_per_pass": 1e3 * el / n}
 
 
 # ---------------------------------------------------------------------------
@@ -537,7 +646,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="time the step as eight eager launches instead of one CUDA graph replay")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="seconds of oracle passes for the cpu_baseline leg (at least one pass)")
+    ap.add_argument("--oracle-rows", type=int, default=0,
+                    help="contiguous tokens of the workload per oracle pass (default: 4096 for "
+                         "cpu_baseline; for --impl reference at most 4096, fewer when the run's "
+                         "passes would not fit in a few minutes)")
     ap.add_argument("--op", choices=OPS, default=None,
                     help="time one operator alone (also the driver for ncu captures)")
     ap.add_argument("--tokens", type=int, default=0,
@@ -566,22 +680,16 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        rows = 256
-        small, inp = oracle_sample_inputs(wl, rows)
-        for _ in range(args.warmup):
-            oracle_step(small, inp)
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            oracle_step(small, inp)
-        el = time.perf_counter() - t0
-        value = args.steps * rows / el
+        # each step: one pass of the oracle over a contiguous block of the workload
+        rows = args.oracle_rows or reference_rows(wl, args.steps + args.warmup)
+        cb = time_oracle(wl, rows, 0.0, passes=args.steps, warmup=args.warmup)
+        value = cb["value"]
+        cb["sample"] = "each step: " + cb["sample"]
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["ms_per_pass"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "impl": "reference", "config": config,
-                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                 "sample": f"each step: all 8 operators over {rows} tokens of {wl.name} "
-                                           "(same widths), float64 numpy, single thread"},
+                "cpu_baseline": cb,
                 "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -712,7 +820,7 @@ def main():
     # Bit 1 is set by a kernel whose bounded wait on its own copies ran out.
     line["device_error_word"] = step.gb.device_error()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = time_oracle(wl, 256, args.cpu_seconds)
+        line["cpu_baseline"] = time_oracle(wl, args.oracle_rows or ORACLE_ROWS, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line))
 

@@ -26,7 +26,11 @@
  *    scratch array of gbln_rmsnorm_bwd_noalloc.  It tracks 64 devices: on a
  *    device with ordinal 64 or above, the calls that need that state (the
  *    backward passes, RoPE, the gated units and activations, the error word)
- *    return GBLN_ERR_CUDA.
+ *    return GBLN_ERR_CUDA.  That state is looked up once per device and kept for
+ *    the life of the process, so the device's primary context must not be torn
+ *    down (cudaDeviceReset, or the driver API's primary-context reset) while the
+ *    library is in use: after a reset the cached addresses (error word, scratch
+ *    array) and shared-memory limits no longer hold.
  *  - Layout: row-major and contiguous.  "[T, H]" means T rows of H elements.
  *  - Streams: work is enqueued on `stream` (NULL = the legacy default stream) and
  *    the call returns without synchronising.  Errors raised by the kernels
@@ -197,7 +201,10 @@ gbln_status gbln_rmsnorm_dw_finalize(const float* dw_partial, int64_t P, int64_t
  * gbln_rmsnorm_bwd's by float32 rounding.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.
+ * any stream capture.  The address is kept until the process exits: resetting
+ * the device's primary context (cudaDeviceReset) while the library is loaded
+ * moves the array, and later calls would write through the stale address, so
+ * do not reset a device that this entry point has been called on.
  * Errors: as gbln_rmsnorm_bwd; GBLN_ERR_WORKSPACE if H > 4 Mi (a partial row
  * would not fit); GBLN_ERR_CUDA if the address lookup fails.  T == 0 sets dw to
  * zero (one launch).  dx may alias dy or dresidual_out exactly.

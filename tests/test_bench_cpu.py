@@ -22,16 +22,21 @@ def _check(line, n_gpus):
     assert line["impl"] == "reference" and line["n_gpus"] == n_gpus
     assert line["unit"] == "tokens/s" and line["value"] > 0 and line["higher_is_better"] is True
     assert line["steps"] == 2 and line["warmup"] == 3
-    assert line["config"]["workload"] == "qwen3_0p6b"
+    assert line["config"]["workload"] == "llama3_8b_packed_outliers"
     cb = line["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"] and cb["sample"]
+    assert cb["rows"] == 512 and cb["passes"] == 2 and cb["cpu_model"] and cb["host_logical_cores"] >= 1
+    assert cb["tokens_per_s_label"] == "extrapolated" and "extrapolated" in cb["sample"]
+    assert set(cb["per_operator"]) == {"positions", "rmsnorm_fwd", "rope_fwd", "swiglu_fwd", "swiglu_bwd",
+                                       "rope_bwd", "rmsnorm_bwd"}
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
 
 
 def test_reference_arm_one_process():
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3"],
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3",
+                        "--oracle-rows", "512"],
                        cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     lines = _lines(r.stdout)
@@ -45,7 +50,8 @@ def test_reference_arm_under_torchrun_prints_once():
         port = s.getsockname()[1]
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port),
-           "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "3"]
+           "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "3",
+           "--oracle-rows", "512"]
     env = dict(os.environ, OMP_NUM_THREADS="1")
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
     assert r.returncode == 0, r.stderr[-2000:]

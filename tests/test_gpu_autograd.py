@@ -62,6 +62,8 @@ def test_autograd_layer_chain():
     pos = torch.arange(T, dtype=torch.int32, device="cuda") % 20
     table = gb.rope_table(20, D, 1e4)
     y = ga.rms_norm(x, w, 1e-5)
+    seen = {}
+    y.register_hook(lambda g: seen.__setitem__("dY", g.detach().clone()))  # what the backward receives
     q, k = ga.rotary((y @ wq).view(T, Hq, D), (y @ wk).view(T, Hk, D), pos, table)
     out = ga.swiglu(y @ wg, y @ wu)
     cq, ck, co = _randn((T, Hq, D), dt, 17), _randn((T, Hk, D), dt, 18), _randn((T, I), dt, 19)
@@ -80,7 +82,13 @@ def test_autograd_layer_chain():
     dK = oracle.rope_bwd(to64(ck), p, 1e4).reshape(T, Hk * D)
     dY = dQ @ WQ.T + dK @ WK.T + dG @ WG.T + dU @ WU.T
     dX, dW = oracle.rmsnorm_bwd(dY, None, X, W, 1e-5)
-    check_io(to64(x.grad), dX, "f32", "x.grad", scale=np.max(np.abs(dY)) * 4)
+    # The float32 GEMMs between the operators round dY (they are torch's, not this
+    # library's), so x.grad is held to the stated float32 bound against the
+    # oracle's backward of the dY the wrapper actually received, and to the
+    # weight-gradient bound against the float64 chain.
+    dX_seen, _ = oracle.rmsnorm_bwd(to64(seen["dY"]), None, X, W, 1e-5)
+    check_io(to64(x.grad), dX_seen, "f32", "x.grad")
+    check_dw(to64(x.grad).ravel(), dX.ravel(), "x.grad (float64 chain)")
     check_dw(to64(w.grad), dW, "weight.grad")
     check_dw(to64(wg.grad), Y.T @ dG, "wg.grad")
     check_dw(to64(wq.grad), Y.T @ dQ, "wq.grad")

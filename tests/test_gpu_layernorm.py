@@ -9,7 +9,7 @@ import torch
 import oracle
 import rmsnorm_fwd_bwd_03_gb300 as gb
 
-from _checks import check_dw, check_io, check_rstd, to64
+from _checks import check_dw, check_io, check_rstd, dx_scale, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -28,11 +28,6 @@ def _randn(shape, dtype, seed, scale=1.0, shift=0.0, offset=0):
     n = int(np.prod(shape))
     buf = torch.randn(n + offset, generator=g, device="cuda") * scale + shift
     return buf.to(dtype)[offset:].view(shape)
-
-
-def _dx_scale(dy, w, rstd, dres):
-    s = np.max(np.abs(dy * w) * rstd[:, None]) * 3 if dy.size else 0.0  # three terms of similar size
-    return s + (np.max(np.abs(dres)) if dres is not None else 0.0)
 
 
 @pytest.mark.parametrize("T,H", [(1, 1), (3, 13), (5, 8), (7, 896), (33, 1000), (2, 1024), (17, 4100),
@@ -66,7 +61,7 @@ def test_layernorm_shapes(T, H, io, wt, opts, offset):
     assert np.allclose(to64(mean), mean_ref, rtol=1e-5, atol=1e-6 * np.max(np.abs(h_ref)))
     dres64 = None if dres is None else to64(dres)
     dx_ref, dw_ref, db_ref = oracle.layernorm_bwd(to64(dy), dres64, h_ref, w64, eps)
-    check_io(to64(dx), dx_ref, io, "dx", scale=_dx_scale(to64(dy), w64, rstd_ref, dres64))
+    check_io(to64(dx), dx_ref, io, "dx", scale=dx_scale(to64(dy), w64, rstd_ref, dres64, terms=3))
     if H > 1:
         check_dw(to64(dw), dw_ref, "dW")
     else:
