@@ -24,18 +24,38 @@ namespace {
 
 constexpr int kGluBlock = 256;
 
-// sigmoid(g) = 1 / (1 + exp(-g)).  float32 I/O uses the accurate expf and an
-// IEEE division.  bf16 I/O moves only 2 bytes per element, so the arithmetic
-// per element must stay within a few instructions for the kernel to remain
-// HBM-bound: the fast exponential and the fast division (relative errors of a
-// few float32 ulp, far below bf16 rounding).  For g < ~-88, exp(-g) = inf and
-// both forms give 0 (the fast division returns 0 for divisors beyond 2^126).
+// bf16 I/O moves only 2 bytes per element, so the arithmetic per element must
+// stay within a few instructions for the kernels to remain HBM-bound.  Their
+// exponentials and reciprocals therefore go straight to the hardware's base-2
+// exponential and reciprocal approximations in flush-to-zero form
+// (ex2.approx.ftz, rcp.approx.ftz), with e^a = 2^(a log2 e).  Their relative
+// errors are a few float32 ulp, far below bf16 rounding, and none of the
+// formulas needs denormals (a denormal exponential or reciprocal is far below
+// bf16 resolution wherever it appears); dropping the denormal handling saves
+// instructions.  float32 I/O keeps the accurate library functions.
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_ftz(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// e^a for the bf16 paths (a * log2 e rounded once, then ex2).
+__device__ __forceinline__ float exp_fast(float a) { return ex2_ftz(a * kLog2e); }
+
+// sigmoid(g) = 1 / (1 + exp(-g)): expf and an IEEE division for float32 I/O.
+// For g < ~-88, exp(-g) = inf and both forms give 0 (the reciprocal of inf is 0).
 template <typename T>
 __device__ __forceinline__ float sigmoid(float g) {
   if constexpr (sizeof(T) == 4) {
     return 1.0f / (1.0f + expf(-g));
   } else {
-    return __fdividef(1.0f, 1.0f + __expf(-g));
+    return rcp_ftz(1.0f + exp_fast(-g));
   }
 }
 
@@ -61,8 +81,8 @@ constexpr float kAsA1 = 0.254829592f, kAsA2 = -0.284496736f, kAsA3 = 1.421413741
 
 __device__ __forceinline__ float gauss_cdf_as(float x, float& ex) {
   const float z = fabsf(x) * kInvSqrt2;
-  const float t = __fdividef(1.0f, fmaf(kAsP, z, 1.0f));
-  ex = __expf(-z * z);
+  const float t = rcp_ftz(fmaf(kAsP, z, 1.0f));
+  ex = exp_fast(-z * z);
   const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, kAsA5, kAsA4), kAsA3), kAsA2), kAsA1);
   const float half_erfc = 0.5f * poly * ex;
   return x >= 0.f ? 1.0f - half_erfc : half_erfc;
@@ -73,7 +93,7 @@ template <typename T, int ACT>
 __device__ __forceinline__ float act_f(float x) {
   if constexpr (ACT == GBLN_ACT_SILU) {
     if constexpr (sizeof(T) == 4) return x / (1.0f + expf(-x));
-    else return __fdividef(x, 1.0f + __expf(-x));
+    else return x * rcp_ftz(1.0f + exp_fast(-x));
   } else if constexpr (ACT == GBLN_ACT_GELU_TANH) {
     return x * sigmoid<T>(kGeluK * (x + kGeluC * x * x * x));
   } else if constexpr (ACT == GBLN_ACT_GELU_ERF) {

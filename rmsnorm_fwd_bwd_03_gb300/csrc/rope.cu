@@ -11,8 +11,10 @@
 //
 // HBM-bound design: each element is read and written exactly once (in place is
 // allowed); cos/sin come from a float32 table built once in double precision.
-// The main path is a warp-specialised TMA pipeline (see rope_staged_kernel);
-// a register path covers layouts it does not take.
+// The main path is one warp per (token, chunk of head rows) with the token's
+// cos/sin held in registers across the rows a lane rotates (rope_warp_kernel);
+// tokens with many heads per lane take a warp-specialised TMA pipeline
+// (rope_staged_kernel); a register path covers layouts neither takes.
 
 #include <atomic>
 
@@ -264,6 +266,66 @@ rope_kernel(const RopeArgs<T> A, int HP) {
 }
 
 // ---------------------------------------------------------------------------
+// Warp path: one warp per (token, chunk of head rows), nothing staged.  With nu
+// units per head row (a unit as in the register path) dividing 32, lane
+// (g, v) = (lane / nu, lane % nu) owns unit v of the chunk's head rows g,
+// g + G, g + 2G, ... (G = 32 / nu), at most kWarpHeads of them.  The lane reads
+// its token's cos/sin entries for unit v once (VEC pairs straight into
+// registers) and rotates every head row it owns with them, so the table costs
+// 64 bytes per lane and token instead of 64 bytes per 32 bytes of Q/K.  All of
+// a lane's row loads are issued before the first is used; for fixed j the warp
+// covers G consecutive head rows, so each load instruction touches whole
+// 128-byte segments.  No loop and no shared memory: the block scheduler keeps
+// enough warps resident to cover DRAM latency.
+// ---------------------------------------------------------------------------
+constexpr int kWarpHeads = 6;
+
+template <typename T, bool BWD, bool IL>
+__global__ void __launch_bounds__(256, 3)
+rope_warp_kernel(const RopeArgs<T> A, int nchunk, int ch) {
+  constexpr int VEC = VecOf<T>::N;
+  constexpr int NP = IL ? VEC / 2 : VEC;  // cos/sin pairs of a unit
+  const int half = A.D / 2, HT = A.Hq + A.Hk;
+  const int nu = IL ? A.D / VEC : half / VEC;
+  const int G = 32 / nu;
+  const int lane = threadIdx.x & 31;
+  const int v = lane % nu, g = lane / nu;
+  const int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t t = item / nchunk;
+  if (t >= A.rows) return;  // uniform per warp
+  const int c = (int)(item - t * nchunk);
+  const int i0 = v * VEC, c0 = IL ? i0 / 2 : i0;
+  const int hb = g + G * c * ch;
+  const int p = __ldg(A.pos + t);
+  Packed<T, VEC> a[kWarpHeads], b[kWarpHeads];
+#pragma unroll
+  for (int j = 0; j < kWarpHeads; ++j) {
+    const int h = hb + G * j;
+    if (j < ch && h < HT) {
+      const T* src = A.src(t, h);
+      a[j].load(src + i0);
+      if constexpr (!IL) b[j].load(src + half + i0);
+    }
+  }
+  // out-of-range position: the table is not read, the outputs are NaN and the
+  // device error word records it
+  const bool ok = p >= 0 && (int64_t)p < A.max_pos;
+  if (!ok && lane == 0 && c == 0) atomicOr(A.err, kErrBadPosition);
+  const CsUnit<NP> cs = load_cs<NP, false>(A.cs + (ok ? (size_t)p * half : 0) + c0, ok);
+#pragma unroll
+  for (int j = 0; j < kWarpHeads; ++j) {
+    const int h = hb + G * j;
+    if (j < ch && h < HT) {
+      T* dst = A.dst(t, h);
+      if constexpr (IL)
+        rotate_il_store<T, VEC, BWD>(a[j], cs, dst + i0);
+      else
+        rotate_store<T, VEC, BWD>(a[j], b[j], cs, dst + i0, dst + half + i0);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Staged path: a persistent block walks tiles of TT consecutive tokens.  One
 // producer thread reads the tile's positions and fills a stage of a ring of S
 // shared-memory stages with TMA bulk copies: the tile's Q rows and K rows and
@@ -494,6 +556,20 @@ gbln_status rope_typed(const RopeArgs<T>& A, cudaStream_t s) {
   const int unit = vec ? VEC : (IL ? 2 : 1);
   const int nu = IL ? D / unit : half / unit;
   if (nu > 512) return GBLN_ERR_UNSUPPORTED;  // head size above 1024 (bf16 vector path: 8192)
+  // Warp path: vector layout with a unit count that divides a warp, and at most
+  // two chunks of head rows per lane and token (up to 40 heads of 128 at bf16).
+  // With more (70B widths: 72 heads) the staged pipeline below measured faster.
+  const int G = vec && nu <= 32 && 32 % nu == 0 ? 32 / nu : 0;
+  const int L = G ? (HT + G - 1) / G : 0;  // head rows per lane and token
+  if (G && L <= 2 * kWarpHeads) {
+    const int nchunk = (L + kWarpHeads - 1) / kWarpHeads;
+    const int ch = (L + nchunk - 1) / nchunk;
+    const int64_t blocks = (A.rows * nchunk + 7) / 8;  // 8 warps per block
+    if (blocks <= 0x7fffffffLL) {
+      rope_warp_kernel<T, BWD, IL><<<(unsigned)blocks, 256, 0, s>>>(A, nchunk, ch);
+      return launch_status();
+    }
+  }
   // Staged (TMA bulk) path: vector layout and a token small enough that four
   // stages of at least one token fit two blocks per SM.  In place is fine: a
   // tile is completely in shared memory before any of its outputs is stored.

@@ -346,9 +346,15 @@ def test_swiglu_guard_bands():
     assert go.intact() and gdg.intact() and gdu.intact()
 
 
-@pytest.mark.parametrize("Hq,Hk,D,offset", [(16, 8, 128, 0), (32, 8, 128, 0), (3, 1, 130, 1)])
+# bf16 launch paths: warp kernel with one chunk (24 heads of 128) and two chunks
+# of head rows per lane (40 heads), TMA-staged kernel with several rows per
+# thread and token (72 heads of 128) and one row (24 heads of 96: a head row of
+# six 16-byte units, which does not divide a warp), register kernel (unaligned).
+ROPE_PATHS = [(16, 8, 128, 0), (32, 8, 128, 0), (64, 8, 128, 0), (16, 8, 96, 0), (3, 1, 130, 1)]
+
+
+@pytest.mark.parametrize("Hq,Hk,D,offset", ROPE_PATHS)
 def test_rope_guard_bands(Hq, Hk, D, offset):
-    # staged path (one and several rows per thread and token) and the register path
     T, dt = 23, torch.bfloat16
     q = _randn((T, Hq, D), dt, 85, offset=offset)
     k = _randn((T, Hk, D), dt, 86, offset=offset)
@@ -385,12 +391,14 @@ def test_layernorm_and_mxfp8_guard_bands():
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_rope_out_of_range_with_cos_sin_in_registers(io):
-    # 40 head rows per token: staged threads rotate several rows per token and
-    # hold the token's cos/sin in registers; a bad position must still give NaN
-    # rows and the error bit, and the other tokens the exact rotation.
+@pytest.mark.parametrize("Hq,Hk", [(32, 8), (64, 8)])
+def test_rope_out_of_range_with_cos_sin_in_registers(io, Hq, Hk):
+    # Threads that rotate several head rows per token hold the token's cos/sin
+    # in registers (the warp kernel at 40 heads; with bf16 at 72 heads the
+    # staged kernel); a bad position must still give NaN rows and the error
+    # bit, and the other tokens the exact rotation.
     dt = IO[io]
-    T, Hq, Hk, D = 9, 32, 8, 128
+    T, D = 9, 128
     q = _randn((T, Hq, D), dt, 71)
     k = _randn((T, Hk, D), dt, 72)
     table = gb.rope_table(50, D, 1e6)
@@ -428,9 +436,11 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable():
     check_io(to64(qo), oracle.rope_fwd(to64(q), pos.cpu().numpy(), 1e6), "bf16", "q' after timeout")
 
 
-def test_device_error_word_is_clear_after_staged_kernels():
-    # RoPE's staged path bounds its waits on TMA copies; none may have given up.
-    T, Hq, Hk, D = 4097, 32, 8, 128
+@pytest.mark.parametrize("Hq,Hk,D", [(64, 8, 128), (16, 8, 96)])
+def test_device_error_word_is_clear_after_staged_kernels(Hq, Hk, D):
+    # RoPE's staged path (72 heads of 128; 24 heads of 96) bounds its waits on
+    # TMA copies; none may have given up.
+    T = 4097
     q = _randn((T, Hq, D), torch.bfloat16, 91)
     k = _randn((T, Hk, D), torch.bfloat16, 92)
     pos = torch.arange(T, dtype=torch.int32, device="cuda") % 1000

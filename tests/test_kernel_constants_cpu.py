@@ -37,6 +37,8 @@ def test_gelu_constants_match_their_definitions():
     assert c["kGeluC"] == 0.044715
     assert f32(c["kInvSqrt2"]) == f32(1.0 / math.sqrt(2.0))
     assert f32(c["kInvSqrt2Pi"]) == f32(1.0 / math.sqrt(2.0 * math.pi))
+    # e^a = 2^(a log2 e) in the bf16 exponentials
+    assert f32(c["kLog2e"]) == f32(1.0 / math.log(2.0))
 
 
 def _as_erfc(z, c, dtype):
