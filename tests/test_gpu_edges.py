@@ -182,8 +182,12 @@ def test_rmsnorm_workspace_too_small_and_empty():
 # RoPE
 # ---------------------------------------------------------------------------
 
+# (40, 8, 128) and (44, 8, 128) sit on either side of the warp kernel's limit of
+# 12 head rows per lane for bf16 (48 and 52 heads); (20, 4, 128) and (21, 4, 128)
+# for float32 (24 and 25 heads of 16 units).
 @pytest.mark.parametrize("T,Hq,Hk,D", [(1, 1, 0, 2), (5, 3, 1, 6), (7, 14, 2, 64), (9, 4, 4, 128),
-                                        (33, 2, 1, 256), (3, 1, 1, 18)])
+                                        (33, 2, 1, 256), (3, 1, 1, 18), (5, 40, 8, 128),
+                                        (5, 44, 8, 128), (6, 20, 4, 128), (6, 21, 4, 128)])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("offset", [0, 1])
 def test_rope_shapes(T, Hq, Hk, D, io, offset):
