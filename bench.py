@@ -49,10 +49,14 @@ KERNEL_SOURCE = {"positions": "rope.cu", "rmsnorm_fwd": "rmsnorm.cu", "rope_fwd"
 # operator, with the sha256 of the kernel source they were taken on: a changed
 # kernel reports null until it is captured again.  Summaries live under profiles/.
 NCU_TRAFFIC = {
-    # glu_bwd_vec at Qwen3-0.6B widths, full size: dram__bytes_read.sum + dram__bytes_write.sum,
-    # mean of 12 launches of one one-pass ncu capture (cold L2: ~59 MB of the writes
-    # are still in L2 when a launch ends)
-    ("qwen3_0p6b", "swiglu_bwd"): {"bytes": 302011008 + 142262528, "src_sha": "3ff2bc8ec94f69ba"},
+    # glu_bwd_vec on the packed Llama-3-8B workload: dram__bytes_read.sum + dram__bytes_write.sum
+    # at the same widths with 8192 and 16384 tokens (one launch each, cold L2: 1119069696 and
+    # 2292990208 bytes), extrapolated along that line to 65536 tokens (the full launch is
+    # beyond the size rule for a counter capture; the traffic grows by 143,300 bytes per token)
+    ("llama3_8b_packed_outliers", "swiglu_bwd"): {"bytes": 9336513280, "src_sha": "fd5eda3018b6c936"},
+    # glu_bwd_vec at Qwen3-0.6B widths, the full launch (one capture, cold L2: ~56 MB of the
+    # writes are still in L2 when it ends)
+    ("qwen3_0p6b", "swiglu_bwd"): {"bytes": 302015488 + 145051648, "src_sha": "fd5eda3018b6c936"},
 }
 
 
