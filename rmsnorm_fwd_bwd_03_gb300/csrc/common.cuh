@@ -1,9 +1,9 @@
 // Shared device helpers of libgbln: 128-bit loads / stores and packs of bf16 /
 // f32, fp32 row reductions (warp shuffles, named barriers, compensated sums),
 // the fixed-order column sum that finishes the weight gradients, the MXFP8
-// quantisation epilogue, TMA bulk copies with bounded mbarrier waits, and the
-// host-side argument checks.  Nothing here is used by the CPU oracle, and
-// nothing from it is used here.
+// quantisation epilogue, TMA bulk copies with bounded mbarrier waits, the L2
+// prefetch, and the host-side argument checks.  Nothing here is used by the
+// CPU oracle, and nothing from it is used here.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -235,6 +235,12 @@ struct KahanSum {
     s = t;
   }
 };
+
+// Ask the TMA unit to bring `bytes` at p (16-byte aligned, a multiple of 16)
+// into L2 ahead of use: no completion to wait for, nothing is written.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // Barrier `id` (1..15) over `threads` threads of the block (a multiple of 32).
 __device__ __forceinline__ void bar_sync_named(int id, int threads) {

@@ -290,6 +290,14 @@ ln_bwd_cta(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
   for (int k = 0; k < 2 * NSL; ++k) acc[k * TPR + l] = make_float4(0.f, 0.f, 0.f, 0.f);
 
   for (int64_t row = r0; row < r1; ++row) {  // same trip count in every thread
+    // thread 0 asks for the block's next row in L2 while this one is processed
+    if (l == 0 && row + 1 < r1) {
+      const size_t nb = (size_t)(row + 1) * H;
+      const uint32_t rb = (uint32_t)(H * sizeof(T));
+      prefetch_l2(dy + nb, rb);
+      prefetch_l2(h + nb, rb);
+      if constexpr (DRES) prefetch_l2(dres + nb, rb);
+    }
     const size_t base = (size_t)row * H;
     uint4 dya[VPT], ha[VPT], dra[VPT];
 #pragma unroll

@@ -158,6 +158,18 @@ rms_bwd_vec(const T* dy, const T* dres, const T* h, const W* __restrict__ w,
   // so the __syncthreads inside row_sum is reached by all.  Only the packed
   // inputs stay in registers across the reduction; n and g are recomputed.
   for (int64_t row = r0 + g; row < r1; row += RPC) {
+    // One row per block (wide rows): thread 0 asks for the block's next row in
+    // L2 while this one is processed, so its loads wait on L2, not DRAM.  (For
+    // several rows per block the same prefetch measured slower.)
+    if constexpr (RPC == 1) {
+      if (threadIdx.x == 0 && row + 1 < r1) {
+        const size_t nb = (size_t)(row + 1) * H;
+        const uint32_t rb = (uint32_t)(H * sizeof(T));
+        prefetch_l2(dy + nb, rb);
+        prefetch_l2(h + nb, rb);
+        if constexpr (DRES) prefetch_l2(dres + nb, rb);
+      }
+    }
     const size_t base = (size_t)row * H;
     uint4 dya[VPT], ha[VPT], dra[VPT];
 #pragma unroll
