@@ -50,13 +50,13 @@ KERNEL_SOURCE = {"positions": "rope.cu", "rmsnorm_fwd": "rmsnorm.cu", "rope_fwd"
 # kernel reports null until it is captured again.  Summaries live under profiles/.
 NCU_TRAFFIC = {
     # glu_bwd_vec on the packed Llama-3-8B workload: dram__bytes_read.sum + dram__bytes_write.sum
-    # at the same widths with 8192 and 16384 tokens (one launch each, cold L2: 1119069696 and
-    # 2292990208 bytes), extrapolated along that line to 65536 tokens (the full launch is
-    # beyond the size rule for a counter capture; the traffic grows by 143,300 bytes per token)
-    ("llama3_8b_packed_outliers", "swiglu_bwd"): {"bytes": 9336513280, "src_sha": "fd5eda3018b6c936"},
+    # at the same widths with 8192 and 16384 tokens (one launch each, cold L2: 1118481152 and
+    # 2292602112 bytes), extrapolated along that line to 65536 tokens (the full launch is
+    # beyond the size rule for a counter capture; the traffic grows by 143,325 bytes per token)
+    ("llama3_8b_packed_outliers", "swiglu_bwd"): {"bytes": 9337327872, "src_sha": "e75f3acc8277048b"},
     # glu_bwd_vec at Qwen3-0.6B widths, the full launch (one capture, cold L2: ~56 MB of the
     # writes are still in L2 when it ends)
-    ("qwen3_0p6b", "swiglu_bwd"): {"bytes": 302015488 + 145051648, "src_sha": "fd5eda3018b6c936"},
+    ("qwen3_0p6b", "swiglu_bwd"): {"bytes": 447497216, "src_sha": "e75f3acc8277048b"},
 }
 
 
