@@ -657,7 +657,7 @@ def main():
                          "cpu_baseline; for --impl reference at most 4096, fewer when the run's "
                          "passes would not fit in a few minutes)")
     ap.add_argument("--op", choices=OPS, default=None,
-                    help="time one operator alone (also the driver for ncu captures)")
+                    help="time one operator alone (also the program under ncu captures)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="with --op / --next: use the workload's widths with this many tokens")
     ap.add_argument("--next", action="store_true",
