@@ -255,6 +255,64 @@ class Step:
         ]
 
 
+def _cudart():
+    """The CUDA runtime library this process has loaded (torch's), else the
+    first one on the library path."""
+    import ctypes
+    torch.cuda.init()
+    cands = []
+    try:
+        with open("/proc/self/maps") as f:
+            cands = sorted({ln.split()[-1] for ln in f if "libcudart.so" in ln})
+    except OSError:
+        pass
+    for name in cands + ["libcudart.so.13", "libcudart.so"]:
+        try:
+            lib = ctypes.CDLL(name)
+        except OSError:
+            continue
+        lib.cudaHostAlloc.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, ctypes.c_uint]
+        lib.cudaHostAlloc.restype = ctypes.c_int
+        lib.cudaFreeHost.argtypes = [ctypes.c_void_p]
+        lib.cudaFreeHost.restype = ctypes.c_int
+        return lib
+    raise RuntimeError("bench.py: no CUDA runtime library found for page-locked host buffers")
+
+
+def _host_available():
+    """MemAvailable of this host in bytes (0 if unknown)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    return 0
+
+
+class PinnedHostBuffer:
+    """Page-locked host memory from cudaHostAlloc, viewed as a uint8 CPU tensor
+    (allocated outside torch's caching host allocator, which rounds sizes up to
+    a power of two and keeps the blocks)."""
+
+    def __init__(self, nbytes):
+        import ctypes
+        self._rt = _cudart()
+        self._ptr = ctypes.c_void_p()
+        st = self._rt.cudaHostAlloc(ctypes.byref(self._ptr), ctypes.c_size_t(nbytes), 0)
+        if st != 0 or not self._ptr.value:
+            raise RuntimeError(f"cudaHostAlloc of {nbytes} bytes failed with error {st}")
+        self.tensor = torch.frombuffer((ctypes.c_uint8 * nbytes).from_address(self._ptr.value),
+                                       dtype=torch.uint8)
+
+    def free(self):
+        if self._ptr is not None and self._ptr.value:
+            self.tensor = None
+            self._rt.cudaFreeHost(self._ptr)
+            self._ptr = None
+
+
 def e2e_pipelined(wl, device, steps, warmup, world, seed):
     """Throughput of the step with inputs in pinned host memory and every output
     read back: per step one host-to-device copy of the input arena, the eight
@@ -263,10 +321,24 @@ def e2e_pipelined(wl, device, steps, warmup, world, seed):
     upload and step i-1's download; every step's copies are inside the timed
     region."""
     sets = [Step(wl, device, seed), Step(wl, device, seed)]
-    host_in = torch.empty(sets[0].in_arena.shape, dtype=torch.uint8, pin_memory=True)
-    host_in.copy_(sets[0].in_arena)
+    nin, nout = sets[0].in_arena.numel(), sets[0].out_arena.numel()
+    # A throwaway page-locked block of twice the buffers' size (within half of the
+    # host's available memory, shared by the ranks) is taken first and released once
+    # the buffers are in place.  Measured on GB300 (Grace host): after another
+    # process had run on the host (the oracle's reference arm, the test suite), this
+    # pipeline took 92-107 ms per step of 17.7 GB with the buffers allocated straight
+    # away and 59 ms with the throwaway block first, the rate of a host where no
+    # other process had run (58-60 ms either way there); single copies ran at full
+    # speed in every case.
+    spare_bytes = min(2 * (nin + nout), _host_available() // (2 * world) - (nin + nout))
+    spare = PinnedHostBuffer(spare_bytes) if spare_bytes > 0 else None
+    pin_in = PinnedHostBuffer(nin)
     # one host buffer for the results: the read-backs are ordered on one stream
-    host_out = torch.empty(sets[0].out_arena.shape, dtype=torch.uint8, pin_memory=True)
+    pin_out = PinnedHostBuffer(nout)
+    if spare is not None:
+        spare.free()
+    host_in, host_out = pin_in.tensor, pin_out.tensor
+    host_in.copy_(sets[0].in_arena)
     s_in, s_comp, s_out = (torch.cuda.Stream(device) for _ in range(3))
     calls = [st.calls(s_comp.cuda_stream) for st in sets]
     ev_in = [torch.cuda.Event() for _ in sets]
@@ -303,14 +375,17 @@ def e2e_pipelined(wl, device, steps, warmup, world, seed):
     e1.record(s_out)
     torch.cuda.synchronize()
     ms = reduce_max(e0.elapsed_time(e1), world)
-    h2d = sets[0].in_arena.numel()
-    d2h = sets[0].out_arena.numel()
+    h2d, d2h = nin, nout
+    del host_in, host_out
+    pin_in.free()
+    pin_out.free()
     return {"value": world * wl.T * steps / (ms * 1e-3), "unit": "tokens/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "ms_per_step": ms / steps,
-            "method": "one pinned H2D copy of the input arena, the 8 C-ABI calls and one D2H "
-                      "copy of the output arena per step; copies on their own streams overlap "
-                      "the neighbouring steps' kernels (two device buffer sets)"}
+            "method": "one H2D copy of the input arena from page-locked host memory (cudaHostAlloc), "
+                      "the 8 C-ABI calls and one D2H copy of the output arena per step; copies on "
+                      "their own streams overlap the neighbouring steps' kernels (two device buffer "
+                      "sets)"}
 
 
 def run_calls(calls, events=None):
