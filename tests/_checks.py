@@ -2,7 +2,9 @@
 
 Bounds (written here, used everywhere):
   * float32 I/O: normwise maximum relative error  max|gpu - ref| / max|ref| <= 1e-5
-    (elementwise relative error is ill-posed where outputs cross zero);
+    (elementwise relative error is ill-posed where outputs cross zero); only the
+    normalisation dX of rows of at most DX_TERM_SCALE_MAX_H (16) channels is
+    normalised by its largest term instead (``dx_scale``);
   * bf16 I/O: elementwise |gpu - ref| <= 1e-2 * |ref| + 1e-3, against the float64
     oracle value before any rounding to bf16;
   * RMSNorm weight gradient (float32 [H]): ||gpu - ref||_2 / ||ref||_2 <= 1e-3;
