@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from _checks import Guarded, check_dw, check_io, check_mxfp8, check_rstd
+from _checks import DX_TERM_SCALE_MAX_H, Guarded, check_dw, check_io, check_mxfp8, check_rstd, dx_scale
 
 
 def _ref(shape=(8, 64), seed=0):
@@ -91,3 +91,29 @@ def test_guarded_band_detects_a_write_outside_the_region():
     h = Guarded((16,), torch.bfloat16, device="cpu")
     h.raw[h.band - 1] = 2.0     # one element before the start
     assert not h.intact()
+
+
+def test_f32_dx_uses_max_ref_beyond_sixteen_channels():
+    # The largest-term normaliser is only offered for rows of at most 16
+    # channels; at the workload widths dX is held to 1e-5 of max|dx_ref|.
+    rng = np.random.default_rng(5)
+    for H, term in ((1, True), (DX_TERM_SCALE_MAX_H, True), (DX_TERM_SCALE_MAX_H + 1, False), (896, False)):
+        T = 7
+        x, dy, dres = rng.normal(size=(T, H)), rng.normal(size=(T, H)), rng.normal(size=(T, H))
+        w = 1 + 0.1 * rng.normal(size=H)
+        _, h, rstd = oracle.rmsnorm_fwd(x, None, w, 1e-5)
+        dx_ref, _ = oracle.rmsnorm_bwd(dy, dres, h, w, 1e-5)
+        sc = dx_scale(dy, w, rstd, dres)
+        assert (sc is not None) == term, (H, sc)
+        if not term:
+            bad = dx_ref.copy()
+            bad.flat[3] += 1.5e-5 * np.max(np.abs(dx_ref))
+            with pytest.raises(AssertionError, match="normwise"):
+                check_io(bad, dx_ref, "f32", f"dx H={H}", scale=sc)
+            ok = dx_ref.copy()
+            ok.flat[3] += 0.9e-5 * np.max(np.abs(dx_ref))
+            check_io(ok, dx_ref, "f32", f"dx H={H}", scale=sc)
+    # LayerNorm's three terms at 16 channels, none beyond
+    dy16 = rng.normal(size=(3, 16))
+    assert dx_scale(dy16, np.ones(16), np.ones(3), terms=3) == pytest.approx(3 * np.max(np.abs(dy16)))
+    assert dx_scale(rng.normal(size=(3, 17)), np.ones(17), np.ones(3), terms=3) is None
