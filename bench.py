@@ -313,6 +313,19 @@ class PinnedHostBuffer:
             self._ptr = None
 
 
+def _same_chunks(host, dev, chunks=16, chunk_bytes=16 << 20):
+    """Byte equality of a host and a device uint8 buffer of the same size on
+    `chunks` evenly spaced chunks (the whole buffer when it is small)."""
+    n = host.numel()
+    if dev.numel() != n:
+        return False
+    if n <= chunks * chunk_bytes:
+        return torch.equal(host, dev.cpu())
+    step = (n - chunk_bytes) // (chunks - 1)
+    return all(torch.equal(host[o:o + chunk_bytes], dev[o:o + chunk_bytes].cpu())
+               for o in range(0, n - chunk_bytes + 1, step)[:chunks])
+
+
 def e2e_pipelined(wl, device, steps, warmup, world, seed):
     """Throughput of the step with inputs in pinned host memory and every output
     read back: per step one host-to-device copy of the input arena, the eight
@@ -376,12 +389,17 @@ def e2e_pipelined(wl, device, steps, warmup, world, seed):
     torch.cuda.synchronize()
     ms = reduce_max(e0.elapsed_time(e1), world)
     h2d, d2h = nin, nout
+    # The copies moved the right bytes: sampled chunks of the last step's read-back
+    # equal its device output arena, and both device input arenas equal the host's.
+    last = (steps - 1) % 2
+    verified = (_same_chunks(host_out, sets[last].out_arena) and
+                all(_same_chunks(host_in, st.in_arena) for st in sets))
     del host_in, host_out
     pin_in.free()
     pin_out.free()
     return {"value": world * wl.T * steps / (ms * 1e-3), "unit": "tokens/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
-            "ms_per_step": ms / steps,
+            "ms_per_step": ms / steps, "readback_verified": bool(verified),
             "method": "one H2D copy of the input arena from page-locked host memory (cudaHostAlloc), "
                       "the 8 C-ABI calls and one D2H copy of the output arena per step; copies on "
                       "their own streams overlap the neighbouring steps' kernels (two device buffer "
